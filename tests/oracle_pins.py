@@ -1,0 +1,436 @@
+"""Pins for the oracle: checks against facts that do not come from the oracle.
+
+Each pin is a function of the loaded oracle library (a ctypes handle), so the
+same pins run against the real oracle (``test_oracle_pins.py``) and against
+copies with a planted mistake (``test_oracle_mutants.py``), which must fail at
+least one of them.
+
+What pins what:
+  - first-step closed form: with m = v = 0 and t = 1 the bias-corrected
+    update is lr * g / (|g| + eps) (the textbook AdamW reduces to it);
+  - constant-gradient closed form: for a gradient held fixed, m_t = (1 -
+    beta1^t) g and v_t = (1 - beta2^t) g^2, so every step moves w by
+    lr * g / (|g| + eps);
+  - weight decay closed form: w (1 - lr wd) - lr g / (|g| + eps);
+  - two-step closed form with two different gradients, written out;
+  - clip: a vector of one repeated value has norm |a| sqrt(N);
+  - norm: index-order binary64 sum vs math.fsum (correctly rounded);
+  - averaging and loss scale on integer-valued gradients (exact);
+  - skip: state bit-identical after a non-finite gradient;
+  - bf16 rounding vs the torch cast; E4M3 values vs torch's float8_e4m3fn;
+    the encoder vs a nearest-value table search with ties to even;
+  - the MX scale rule on blocks built by hand from the format;
+  - shard layout invariants; identical learning (sharded == unsharded);
+  - resume (set_step) reproduces an uninterrupted run;
+  - power-of-two loss-scale invariance of the whole step.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+import oracle
+
+F32 = np.float32
+
+
+def _ulp(x: float) -> float:
+    return float(np.spacing(np.abs(F32(x))))
+
+
+def _bf16(x) -> np.ndarray:
+    """Exact bf16 patterns for values that are exactly representable."""
+    a = np.asarray(x, dtype=np.float32)
+    u = a.view(np.uint32)
+    assert np.all((u & 0xFFFF) == 0), "value not exactly representable in bf16"
+    return (u >> 16).astype(np.uint16)
+
+
+def _trunc(x) -> np.ndarray:
+    """bf16 patterns of float32 values truncated to bf16 (low half dropped):
+    test inputs that are bf16 by construction."""
+    return (np.asarray(x, dtype=np.float32).view(np.uint32) >> 16).astype(np.uint16)
+
+
+def _sp(x) -> np.ndarray:
+    """binary32 spacing at |x|, as float64."""
+    return np.spacing(np.abs(np.asarray(x, dtype=np.float64)).astype(np.float32)).astype(np.float64)
+
+
+def _opt(lib, w0, **hp):
+    return oracle.OracleOptimizer(np.asarray(w0, dtype=np.float32), oracle.Hparams(**hp), lib=lib)
+
+
+# ------------------------------------------------------------- AdamW
+
+def pin_first_step_closed_form(lib):
+    gvals = np.array([1e-3, -2.5e-3, 3e-6, -7e-8, 1e-8, -1e-8, 0.75, -12.0, 4e-9, 0.0], dtype=np.float32)
+    g = _trunc(gvals)
+    gb = oracle.bf16_to_f32(g).astype(np.float64)
+    lr, eps = 1e-3, 1e-8
+    opt = _opt(lib, np.zeros(g.size), lr=lr, eps=eps, weight_decay=0.0, max_grad_norm=0.0)
+    d = opt.step([g], 1.0)
+    assert not d.found_inf and opt.t == 1
+    expect = -lr * gb / (np.abs(gb) + eps)
+    for got, want in zip(opt.w, expect):
+        assert abs(float(got) - want) <= 2 * _ulp(want) + 1e-45, (got, want)
+    # m and v after one step: (1 - beta) times g and g^2
+    assert np.allclose(opt.m, 0.1 * gb, rtol=2e-7, atol=0)
+    assert np.allclose(opt.v, 0.001 * gb * gb, rtol=4e-7, atol=1e-45)
+
+
+def pin_first_step_weight_decay(lib):
+    rng = np.random.default_rng(11)
+    w0 = (rng.standard_normal(64) * 0.02).astype(np.float32)
+    g = _trunc(rng.standard_normal(64).astype(np.float32) * F32(1e-3))
+    gb = oracle.bf16_to_f32(g).astype(np.float64)
+    lr, wd, eps = 1e-3, 0.01, 1e-8
+    opt = _opt(lib, w0, lr=lr, weight_decay=wd, eps=eps, max_grad_norm=0.0)
+    opt.step([g], 1.0)
+    w0d = w0.astype(np.float64)
+    dw = -lr * gb / (np.abs(gb) + eps)
+    expect = w0d * (1.0 - lr * wd) + dw
+    err = np.abs(opt.w.astype(np.float64) - expect)
+    # a few roundings on operands of the size of w0 and of the update
+    tol = 2 * (_sp(w0d) + _sp(dw) + _sp(expect))
+    assert np.all(err <= tol), np.max(err / tol)
+
+
+def pin_constant_gradient(lib):
+    """Held gradient: bias correction makes every step the same size."""
+    gvals = np.array([1e-3, -4e-4, 2.0, -3e-7, 5e-9], dtype=np.float32)
+    g = _trunc(gvals)
+    gb = oracle.bf16_to_f32(g).astype(np.float64)
+    lr, eps, b1, b2 = 1e-3, 1e-8, 0.9, 0.999
+    opt = _opt(lib, np.zeros(g.size), lr=lr, eps=eps, weight_decay=0.0, max_grad_norm=0.0)
+    prev = opt.w.astype(np.float64).copy()
+    for t in range(1, 31):
+        opt.step([g], 1.0)
+        assert opt.t == t
+        dw = opt.w.astype(np.float64) - prev
+        prev = opt.w.astype(np.float64).copy()
+        want = -lr * gb / (np.abs(gb) + eps)
+        assert np.all(np.abs(dw - want) <= 2e-5 * np.abs(want) + 1e-9 * lr), (t, dw, want)
+        assert np.allclose(opt.m, (1 - b1 ** t) * gb, rtol=1e-5, atol=0)
+        assert np.allclose(opt.v, (1 - b2 ** t) * gb * gb, rtol=1e-5, atol=1e-45)
+
+
+def pin_two_step_closed_form(lib):
+    rng = np.random.default_rng(5)
+    n = 32
+    w0 = (rng.standard_normal(n) * 0.02).astype(np.float32)
+    g1 = _trunc(rng.standard_normal(n) * 1e-3)
+    g2 = _trunc(rng.standard_normal(n) * 1e-3)
+    a, b = oracle.bf16_to_f32(g1).astype(np.float64), oracle.bf16_to_f32(g2).astype(np.float64)
+    lr, wd, eps, b1, b2 = 1e-3, 0.01, 1e-8, 0.9, 0.999
+    opt = _opt(lib, w0, lr=lr, weight_decay=wd, eps=eps, max_grad_norm=0.0)
+    opt.step([g1], 1.0)
+    opt.step([g2], 1.0)
+    w1 = w0.astype(np.float64) * (1 - lr * wd) - lr * a / (np.abs(a) + eps)
+    m2 = b1 * (1 - b1) * a + (1 - b1) * b
+    v2 = b2 * (1 - b2) * a * a + (1 - b2) * b * b
+    mh, vh = m2 / (1 - b1 ** 2), v2 / (1 - b2 ** 2)
+    dw2 = -lr * mh / (np.sqrt(vh) + eps)
+    w2 = w1 * (1 - lr * wd) + dw2
+    tol = 4 * (_sp(w0) + _sp(w1) + _sp(dw2) + _sp(w2))
+    assert np.all(np.abs(opt.w - w2) <= tol), np.max(np.abs(opt.w - w2) / tol)
+    assert np.allclose(opt.m, m2, rtol=1e-6)
+    assert np.allclose(opt.v, v2, rtol=1e-6)
+
+
+# ------------------------------------------------------------- clip and norm
+
+def pin_clip_constant_vector(lib):
+    """Every gradient element a: the norm is |a| sqrt(N)."""
+    n, a = 4096, 0.125  # norm = 0.125 * 64 = 8
+    g = _bf16(np.full(n, a, dtype=np.float32))
+    opt = _opt(lib, np.zeros(n), weight_decay=0.0, max_grad_norm=1.0)
+    d = opt.step([g], 1.0)
+    assert d.norm == 8.0 and d.sumsq == 64.0
+    want = 1.0 / (8.0 + 1e-6)
+    assert abs(d.clip - want) <= _ulp(want)
+    # clipped moment: m = (1 - beta1) * a * c
+    assert np.allclose(opt.m, 0.1 * a * d.clip, rtol=2e-7)
+    # below the threshold the factor is exactly one
+    opt2 = _opt(lib, np.zeros(n), weight_decay=0.0, max_grad_norm=9.0)
+    assert opt2.step([g], 1.0).clip == 1.0
+    # the clipped gradient has norm max_norm * norm / (norm + 1e-6)
+    assert abs(8.0 * d.clip - 8.0 / (8.0 + 1e-6)) <= 8.0 * _ulp(want)
+
+
+def pin_norm_vs_fsum(lib):
+    rng = np.random.default_rng(3)
+    g = (rng.standard_normal(200_003) * np.exp(rng.uniform(-8, 2, 200_003))).astype(np.float32)
+    sq = (g * g).astype(np.float64)  # binary32 squares, widened
+    exact = math.fsum(sq.tolist())
+    got = oracle.sumsq(g, lib=lib)
+    assert abs(got - exact) <= 1e-12 * exact, (got, exact)
+
+
+def pin_average_and_unscale(lib):
+    """Integer-valued gradients: every order of addition is exact, so the
+    reduce-scatter + unscale must give exactly sum / (L * P)."""
+    rng = np.random.default_rng(7)
+    for p in (1, 2, 3, 4, 8, 16):
+        n = 257
+        ints = rng.integers(-64, 65, size=(p, n))
+        L = 256.0
+        grads = [_bf16((ints[r] * L).astype(np.float32)) for r in range(p)]
+        inv = oracle.inv_scale(L, p, 1, lib=lib)
+        g = oracle.reduce_unscale(grads, 0, n, inv, lib=lib)
+        want = ints.sum(axis=0) / p  # exact in binary32 for these sizes only when P is 2^k
+        if p & (p - 1) == 0:
+            assert np.array_equal(g, want.astype(np.float32))
+        else:
+            assert np.allclose(g, want, rtol=2 * 2 ** -24, atol=0)
+        inv_sum = oracle.inv_scale(L, p, 0, lib=lib)
+        gs = oracle.reduce_unscale(grads, 0, n, inv_sum, lib=lib)
+        assert np.array_equal(gs, ints.sum(axis=0).astype(np.float32))
+
+
+def pin_skip_on_nonfinite(lib):
+    rng = np.random.default_rng(9)
+    n = 100
+    for bad in (np.inf, -np.inf, np.nan):
+        opt = _opt(lib, rng.standard_normal(n) * 0.02)
+        good = _trunc(rng.standard_normal(n) * 1e-3)
+        opt.step([good, good], 1024.0)
+        snap = (opt.w.copy(), opt.m.copy(), opt.v.copy(), opt.p.copy(), opt.t)
+        g2 = good.copy()
+        g2[n - 1] = F32(bad).view(np.uint32) >> 16 if not np.isnan(bad) else 0x7FC0
+        d = opt.step([good, g2], 1024.0)
+        assert d.found_inf and opt.t == snap[4] and d.t == snap[4]
+        for a, b in zip((opt.w, opt.m, opt.v, opt.p), snap[:4]):
+            assert a.tobytes() == b.tobytes()
+        d = opt.step([good, good], 1024.0)
+        assert not d.found_inf and opt.t == snap[4] + 1
+
+
+def pin_loss_scale_invariance(lib):
+    """bf16(x * 2^k) = bf16(x) * 2^k, and the unscale undoes 2^k exactly."""
+    rng = np.random.default_rng(21)
+    n, p = 1000, 4
+    x = [(rng.standard_normal(n) * 1e-3).astype(np.float32) for _ in range(p)]
+    base = [_trunc(xi) for xi in x]
+    w0 = (rng.standard_normal(n) * 0.02).astype(np.float32)
+    res = []
+    for L in (1024.0, 65536.0):
+        grads = [_bf16(oracle.bf16_to_f32(b) * F32(L)) for b in base]
+        opt = _opt(lib, w0)
+        for _ in range(3):
+            opt.step(grads, L)
+        res.append((opt.w.tobytes(), opt.m.tobytes(), opt.v.tobytes(), opt.p.tobytes()))
+    assert res[0] == res[1]
+
+
+# ------------------------------------------------------------- formats
+
+def pin_bf16_rounding_vs_torch(lib):
+    import torch
+
+    rng = np.random.default_rng(1)
+    u = rng.integers(0, 2 ** 32, size=40_000, dtype=np.uint64).astype(np.uint32)
+    ties = (rng.integers(0, 2 ** 16, size=4000).astype(np.uint32) << 16) | 0x8000
+    special = np.array([0, 0x80000000, 0x7F800000, 0xFF800000, 0x7F7FFFFF, 0x7F7F8000, 0x00000001,
+                        0x00008000, 0x00018000, 0x3F808000, 0x3F818000, 0xBF808000], dtype=np.uint32)
+    bits = np.concatenate([u, ties, special])
+    x = bits.view(np.float32)
+    x = x[~np.isnan(x)]
+    want = torch.from_numpy(x.copy()).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    got = oracle.f32_to_bf16(x, lib=lib)
+    assert np.array_equal(got, want)
+
+
+def pin_e4m3_values_vs_torch(lib):
+    import torch
+
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).float().numpy().astype(np.float64)
+    got = np.array([oracle.e4m3_value(int(c), lib=lib) for c in codes])
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+    assert np.array_equal(np.signbit(got[~nan]), np.signbit(ref[~nan]))
+
+
+def _e4m3_table():
+    """Values of the non-negative finite codes 0x00..0x7E, from the format:
+    exponent bias 7, 3 mantissa bits, subnormals at exponent field 0."""
+    vals = []
+    for c in range(0x7F):
+        e, m = c >> 3, c & 7
+        vals.append(m / 8 * 2.0 ** -6 if e == 0 else (1 + m / 8) * 2.0 ** (e - 7))
+    return np.array(vals)
+
+
+def nearest_e4m3(y: np.ndarray) -> np.ndarray:
+    """Brute force: nearest table value, ties to the even code, sign kept."""
+    tab = _e4m3_table()
+    # Distances are exact in binary64 only for moderate magnitudes; every
+    # magnitude above 448 has 448 as its nearest finite value, so cap there
+    # (at 2^20, far above 448, which keeps the search itself deciding).
+    a = np.minimum(np.abs(y), 2.0 ** 20)[:, None]
+    dist = np.abs(a - tab[None, :])
+    best = dist.min(axis=1, keepdims=True)
+    cand = dist == best
+    # among equal-distance candidates prefer the even code
+    even = (np.arange(0x7F) % 2 == 0)[None, :]
+    pick = np.where((cand & even).any(axis=1), np.argmax(cand & even, axis=1), np.argmax(cand, axis=1))
+    return (pick | np.where(np.signbit(y), 0x80, 0)).astype(np.uint8)
+
+
+def pin_e4m3_encoder_exhaustive(lib):
+    """Every finite bf16 value as an encoder input, plus values around each
+    rounding midpoint, against the brute-force nearest search."""
+    bits = np.arange(65536, dtype=np.uint32) << 16
+    x32 = bits.view(np.float32)
+    y = x32[np.isfinite(x32)].astype(np.float64)
+    tab = _e4m3_table()
+    mids = (tab[1:] + tab[:-1]) / 2
+    around = np.concatenate([mids, np.nextafter(mids, 0), np.nextafter(mids, 1), -mids, tab, -tab])
+    ys = np.concatenate([y, around])
+    got = np.array([oracle.e4m3_encode(v, lib=lib) for v in ys], dtype=np.uint8)
+    for lo in range(0, ys.size, 8192):
+        want = nearest_e4m3(ys[lo:lo + 8192])
+        assert np.array_equal(got[lo:lo + 8192], want), lo
+
+
+def pin_mx_scale_rule(lib):
+    """Blocks built by hand from the OCP MX rule (e = floor(log2 amax) - 8)."""
+    def block(vals):
+        v = np.zeros(32, dtype=np.float32)
+        v[: len(vals)] = vals
+        return _bf16(v)
+
+    for k in (-3, 0, 5):
+        codes, sc = oracle.mx_encode(block([448.0 * 2.0 ** k, -1.0 * 2.0 ** k]), lib=lib)
+        assert sc[0] == 127 + k and codes[0] == 0x7E and codes[1] == 0xB8  # -1.0 = 0x80|(7<<3)
+        # the largest bf16 below 512 shares the binade and saturates to 448
+        codes, sc = oracle.mx_encode(block([510.0 * 2.0 ** k]), lib=lib)
+        assert sc[0] == 127 + k and codes[0] == 0x7E
+        codes, sc = oracle.mx_encode(block([256.0 * 2.0 ** k]), lib=lib)
+        assert sc[0] == 127 + k and codes[0] == 0x78
+    # amax 1.0: e = -8; 2^-17 -> y = 2^-9 (smallest subnormal); 2^-18 -> tie -> 0;
+    # 3 * 2^-19 -> y = 1.5 * 2^-10 -> 2^-9; -2^-20 -> -0
+    codes, sc = oracle.mx_encode(block([1.0, 2.0 ** -17, 2.0 ** -18, 3 * 2.0 ** -19, -(2.0 ** -20)]), lib=lib)
+    assert sc[0] == 119
+    assert list(codes[:5]) == [0x78, 0x01, 0x00, 0x01, 0x80]  # 1.0 * 2^8 = 256 -> 0x78
+    # all zero, and negative zero keeps its sign
+    z = block([])
+    z[3] = 0x8000
+    codes, sc = oracle.mx_encode(z, lib=lib)
+    assert sc[0] == 0 and codes[3] == 0x80 and codes[0] == 0
+    # bf16 subnormals only: the scale clamps at 2^-127, 2^-133 * 2^127 = 2^-6
+    sub = np.zeros(32, dtype=np.uint16)
+    sub[0], sub[1] = 0x0001, 0x0040  # 2^-133 and 2^-127
+    codes, sc = oracle.mx_encode(sub, lib=lib)
+    assert sc[0] == 0 and codes[0] == 0x08 and codes[1] == 0x38  # 2^-6 and 2^0
+    # any infinity or NaN poisons the block
+    for bad in (0x7F80, 0xFF80, 0x7FC0):
+        x = block([1.0])
+        x[7] = bad
+        codes, sc = oracle.mx_encode(x, lib=lib)
+        assert sc[0] == 0xFF and np.all(codes == 0x7F)
+        assert math.isnan(oracle.mx_decode(0x00, 0xFF, lib=lib))
+    # a ragged tail block: missing elements count as zero; amax 3 -> e = -7,
+    # 3 * 2^7 = 384 = 1.5 * 2^8 -> 0x7C, -0.5 * 2^7 = -2^6 -> 0x80 | (13 << 3)
+    codes, sc = oracle.mx_encode(_bf16(np.array([3.0, -0.5], dtype=np.float32)), lib=lib)
+    assert sc.size == 1 and sc[0] == 127 - 7 and list(codes) == [0x7C, 0xE8]
+    # decode multiplies by 2^(s-127), down to the subnormal scale 2^-127
+    assert oracle.mx_decode(0x01, 0, lib=lib) == 2.0 ** -136
+    assert oracle.mx_decode(0x7E, 246, lib=lib) == 448.0 * 2.0 ** 119
+
+
+def pin_mx_loss_scale_shifts_scale_only(lib):
+    import zero_sharded_mixed_flat_gb300.synth as synth
+
+    x = synth.random_bf16(32 * 50, seed=4, scale=1e-3, dist="student_t")
+    xf = oracle.bf16_to_f32(x)
+    c1, s1 = oracle.mx_encode(x, lib=lib)
+    c2, s2 = oracle.mx_encode(_bf16(xf * F32(1024.0)), lib=lib)
+    assert np.array_equal(c1, c2)
+    assert np.array_equal(s2.astype(int) - s1.astype(int), np.full(s1.size, 10))
+
+
+# ------------------------------------------------------------- sharding
+
+def pin_shard_layout(lib):
+    for n in (1, 31, 32, 33, 1000, 65_549, 124_439_808, 3_000_000_000):
+        for p in (1, 2, 3, 4, 7, 8, 16):
+            s = oracle.shard_len(n, p, lib=lib)
+            assert s % 32 == 0 and p * s >= n and s >= -(-n // p) and s < -(-n // p) + 32
+
+
+def pin_identical_learning(lib):
+    """Zero From Scratch, item 19: the sharded (stage-two) step learns exactly
+    what the unsharded step learns, for every P, over ten steps."""
+    rng = np.random.default_rng(13)
+    n = 1013
+    w0 = (rng.standard_normal(n) * 0.02).astype(np.float32)
+    for p in (1, 2, 3, 4, 8):
+        a = _opt(lib, w0, max_grad_norm=0.0)
+        b = _opt(lib, w0, max_grad_norm=0.0)
+        for _ in range(10):
+            grads = [_trunc(rng.standard_normal(n) * 1e-3 * 1024) for _ in range(p)]
+            da = a.step(grads, 1024.0)
+            db = b.step(grads, 1024.0, sharded=True)
+            assert da.found_inf == db.found_inf
+            assert abs(da.sumsq - db.sumsq) <= 1e-13 * da.sumsq
+        for x, y in ((a.w, b.w), (a.m, b.m), (a.v, b.v), (a.p, b.p)):
+            assert x.tobytes() == y.tobytes(), p
+        assert a.t == b.t == 10
+
+
+def pin_resume(lib):
+    rng = np.random.default_rng(17)
+    n, p = 300, 2
+    w0 = (rng.standard_normal(n) * 0.02).astype(np.float32)
+    steps = [[_trunc(rng.standard_normal(n)) for _ in range(p)] for _ in range(10)]
+    full = _opt(lib, w0)
+    for g in steps:
+        full.step(g, 1024.0)
+    first = _opt(lib, w0)
+    for g in steps[:6]:
+        first.step(g, 1024.0)
+    resumed = _opt(lib, first.w)
+    resumed.m[:], resumed.v[:] = first.m, first.v
+    resumed.set_step(first.t)
+    for g in steps[6:]:
+        resumed.step(g, 1024.0)
+    for x, y in ((full.w, resumed.w), (full.m, resumed.m), (full.v, resumed.v), (full.p, resumed.p)):
+        assert x.tobytes() == y.tobytes()
+    t, b1p, b2p = oracle.counters_at(oracle.Hparams(), 10, lib=lib)
+    assert t == 10 and abs(b1p - 0.9 ** 10) <= 1e-15 and abs(b2p - 0.999 ** 10) <= 1e-15
+
+
+PINS = [
+    pin_first_step_closed_form,
+    pin_first_step_weight_decay,
+    pin_constant_gradient,
+    pin_two_step_closed_form,
+    pin_clip_constant_vector,
+    pin_norm_vs_fsum,
+    pin_average_and_unscale,
+    pin_skip_on_nonfinite,
+    pin_loss_scale_invariance,
+    pin_bf16_rounding_vs_torch,
+    pin_e4m3_values_vs_torch,
+    pin_e4m3_encoder_exhaustive,
+    pin_mx_scale_rule,
+    pin_mx_loss_scale_shifts_scale_only,
+    pin_shard_layout,
+    pin_identical_learning,
+    pin_resume,
+]
+
+
+def run_all(lib) -> list[str]:
+    """Run every pin; return the names of those that failed (used on mutants)."""
+    failed = []
+    for pin in PINS:
+        try:
+            pin(lib)
+        except Exception:  # a mutant may also raise instead of failing an assert
+            failed.append(pin.__name__)
+    return failed
