@@ -1,0 +1,421 @@
+"""Benchmark: the sharded mixed-precision optimizer step on one GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload flat16m_p8] [--variant ldg|tma]
+
+A step is one whole optimizer step of the library on one batch of resident
+synthetic inputs: the norm pass (reduce-scatter + unscale + global norm +
+found-inf + clip decision) and the fused shard step (reduce-scatter +
+unscale + clip + AdamW on fp32 w/m/v + bf16 all-gather) over all P
+simulated ranks. Default workload: N = 2^24 parameters, P = 8 ranks, bf16
+gradients N(0, 1e-3) x 1024, AdamW lr 1e-3, betas 0.9/0.999, eps 1e-8,
+wd 0.01, clip 1.0. The working set (0.47 GB) exceeds the 129 MB L2, so no
+flush is needed between steps.
+
+Prints one JSON line (rank 0). ``value`` is parameters updated per second
+over the whole job; ``roofline`` describes the fused shard-step kernel
+against the measured HBM bandwidth; ``e2e`` is the same metric through the
+C ABI with the gradients copied from pinned host memory every step and the
+step scalars read back; ``cpu_baseline`` is the oracle timed on the host.
+
+Under torchrun (N > 1) every GPU runs its own independent P-rank problem (no
+collective on the data path: the simulated ranks live inside one GPU), so
+scaling is weak; the ranks only meet at the barriers around the timed region
+and in the max-over-ranks reduction of the time.
+
+``--impl reference`` times the oracle (the plain CPU statement of the same
+step) on the host cores instead, on a bounded sample of the workload.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "optimizer-step params/sec"
+UNIT = "params/s"
+FALLBACK_HBM_GBS = 6800.0
+SCALARS_D2H_BYTES = 104  # sizeof the device scalar block zg_get_info copies back
+
+
+# --------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """Samples the SM clock and the clock-event reasons of one GPU from a
+    background thread through NVML (the library nvidia-smi uses), reading
+    only. Falls back to polling nvidia-smi when NVML cannot be loaded."""
+
+    REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
+               0x8: "hw_slowdown", 0x10: "sync_boost", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown", 0x100: "display_clock_setting"}
+
+    def __init__(self, cuda_index: int, period_s: float = 0.005):
+        self.period = period_s
+        self.samples: list[tuple[int, int]] = []
+        self.max_mhz = None
+        self._stop = threading.Event()
+        self._thread = None
+        self._nvml = None
+        self._handle = None
+        self._active = False
+        self.source = "none"
+        try:
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                raise OSError("nvmlInit failed")
+            h = ctypes.c_void_p()
+            bus = None
+            try:
+                import torch
+
+                props = torch.cuda.get_device_properties(cuda_index)
+                bus = f"{props.pci_domain_id:08x}:{props.pci_bus_id:02x}:{props.pci_device_id:02x}.0"
+            except Exception:
+                bus = None
+            ok = bus is not None and nv.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ctypes.byref(h)) == 0
+            if not ok and nv.nvmlDeviceGetHandleByIndex_v2(cuda_index, ctypes.byref(h)) != 0:
+                raise OSError("no NVML handle")
+            self._nvml, self._handle = nv, h
+            mx = ctypes.c_uint()
+            if nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:
+                self.max_mhz = int(mx.value)
+            self.source = "nvml"
+        except OSError:
+            self._nvml = None
+            self.source = "nvidia-smi"
+            self._index = cuda_index
+
+    def _read(self):
+        if self._nvml is not None:
+            mhz, rs = ctypes.c_uint(), ctypes.c_ulonglong()
+            self._nvml.nvmlDeviceGetClockInfo(self._handle, 1, ctypes.byref(mhz))
+            fn = getattr(self._nvml, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                self._nvml.nvmlDeviceGetCurrentClocksThrottleReasons
+            fn(self._handle, ctypes.byref(rs))
+            return int(mhz.value), int(rs.value)
+        out = subprocess.run(
+            ["nvidia-smi", f"--id={self._index}", "--query-gpu=clocks.sm,clocks.max.sm,clocks_event_reasons.active",
+             "--format=csv,noheader,nounits"], capture_output=True, text=True, timeout=10).stdout.strip()
+        sm, mx, act = [x.strip() for x in out.split(",")]
+        self.max_mhz = int(mx)
+        return int(sm), int(act, 16)
+
+    def _loop(self):
+        while not self._stop.is_set():
+            try:
+                s = self._read()
+                if self._active:
+                    self.samples.append(s)
+            except Exception:
+                pass
+            time.sleep(self.period if self._nvml is not None else 0.2)
+
+    def start(self):
+        self._thread = threading.Thread(target=self._loop, daemon=True)
+        self._thread.start()
+
+    def region(self, active: bool):
+        self._active = active
+
+    def stop(self) -> dict:
+        self._stop.set()
+        if self._thread:
+            self._thread.join(timeout=5)
+        mhz = [s for s, _ in self.samples]
+        bits = 0
+        for _, r in self.samples:
+            bits |= r
+        reasons = sorted(name for b, name in self.REASONS.items() if bits & b and name != "gpu_idle")
+        return {"sm_mhz": statistics.median(mhz) if mhz else None, "sm_max_mhz": self.max_mhz,
+                "reasons": reasons, "samples": len(mhz), "source": self.source}
+
+
+# --------------------------------------------------------------------- helpers
+
+def measured_peaks() -> tuple[float, str]:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        for key in ("hbm_gbs", "hbm_GBs", "hbm"):
+            if key in d:
+                return float(d[key]), "measured"
+    except (OSError, ValueError):
+        pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "zero_sharded_mixed_flat_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, f), "rb") as fh:
+                h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload: str) -> float | None:
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources (else None)."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            rec = json.load(f).get(f"{kernel}/{workload}")
+    except (OSError, ValueError):
+        return None
+    if not rec or rec.get("src_hash") != kernel_source_hash():
+        return None
+    return float(rec["dram_bytes_per_launch"])
+
+
+def dist_env() -> tuple[int, int, int]:
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int) -> None:
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+# --------------------------------------------------------------------- oracle leg
+
+def time_oracle(workload, budget_s: float, steps: int, warmup: int = 0) -> dict:
+    """Time the oracle's whole step on a contiguous prefix of the flat vector
+    (all P ranks). The prefix length is sized so one step takes about
+    ``budget_s`` on one host core. Returns params/s and the sample used."""
+    import numpy as np
+
+    import oracle
+    from zero_sharded_mixed_flat_gb300 import synth
+
+    def run(ns: int, k: int) -> float:
+        w0 = synth.init_weights(workload, 0, ns)
+        grads = [synth.grads_bf16(workload, 1, r, 0, ns) for r in range(workload.p)]
+        opt = oracle.OracleOptimizer(w0)
+        t0 = time.perf_counter()
+        for _ in range(k):
+            opt.step(grads, workload.loss_scale)
+        return time.perf_counter() - t0
+
+    probe = min(workload.n, 1 << 16)
+    rate = probe / max(run(probe, 2) / 2, 1e-9)
+    ns = int(min(workload.n, max(4096, rate * budget_s)))
+    ns = max(32, ns // 32 * 32)
+    if warmup:
+        run(ns, warmup)
+    el = run(ns, steps)
+    return {"value": ns * steps / el, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"first {ns} of {workload.n} params, all {workload.p} ranks, {steps} steps, one thread",
+            "seconds": el}
+
+
+# --------------------------------------------------------------------- our arm
+
+def bench_ours(args, rank: int, world: int, local: int) -> dict | None:
+    import numpy as np
+    import torch
+
+    from zero_sharded_mixed_flat_gb300 import accounting, synth
+    from zero_sharded_mixed_flat_gb300 import binding as zb
+
+    torch.cuda.set_device(local)
+    wl = synth.workload(args.workload)
+    n, p, ls = wl.n, wl.p, wl.loss_scale
+    total = synth.padded_len(wl)
+    stream = torch.cuda.current_stream()
+
+    # inputs resident in HBM before timing: one step's P gradient buffers
+    host = synth.step_grads(wl, 1)
+    host_t = [torch.from_numpy(h.view(np.int16)).view(torch.bfloat16) for h in host]
+    dev = [h.cuda() for h in host_t]
+    opt = zb.ShardedAdamW(n, p, zb.Hparams(), torch.from_numpy(synth.init_weights(wl)))
+    zb.zg_set_variant(opt.ctx, zb.ZG_VARIANT_TMA if args.variant == "tma" else zb.ZG_VARIANT_LDG)
+
+    for _ in range(args.warmup):
+        opt.step(dev, ls, stream)
+    info = opt.info(stream)
+    assert info.status == 0 and not info.found_inf
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.region(True)
+    t0 = time.perf_counter()
+    for k in range(K):
+        ev[k][0].record(stream)
+        zb.zg_grad_norm(opt.ctx, dev, ls, stream)
+        ev[k][1].record(stream)
+        zb.zg_shard_step(opt.ctx, dev, ls, stream)
+        ev[k][2].record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    clocks.region(False)
+    barrier(world)
+    clk = clocks.stop()
+    info = opt.info(stream)
+    assert info.status == 0 and info.step_t == args.warmup + K, info
+
+    total_ms = ev[0][0].elapsed_time(ev[K - 1][2])
+    norm_ms = sum(ev[k][0].elapsed_time(ev[k][1]) for k in range(K)) / K
+    step_ms = sum(ev[k][1].elapsed_time(ev[k][2]) for k in range(K)) / K
+    t_max = max_over_ranks(total_ms / 1e3, world)
+    value = world * n * K / t_max
+
+    peak, peak_kind = measured_peaks()
+    b_step = accounting.shard_step_bytes_per_param(p) * n
+    b_norm = accounting.grad_norm_bytes_per_param(p) * n
+    achieved = b_step / (step_ms / 1e3) / 1e9
+
+    # e2e: through the C ABI with gradients coming from pinned host memory
+    # every step and the step scalars read back every step.
+    pinned = [h.pin_memory() for h in host_t]
+    e2e_steps = max(3, min(K, 200))
+    for k in range(2):
+        for r in range(p):
+            dev[r].copy_(pinned[r], non_blocking=True)
+        opt.step(dev, ls, stream)
+        opt.info(stream)
+    barrier(world)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for k in range(e2e_steps):
+        for r in range(p):
+            dev[r].copy_(pinned[r], non_blocking=True)
+        opt.step(dev, ls, stream)
+        opt.info(stream)  # device->host read of the step result; synchronises
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_s = max_over_ranks(e0.elapsed_time(e1) / 1e3, world)
+    e2e = {"value": world * n * e2e_steps / e2e_s, "unit": UNIT, "steps": e2e_steps,
+           "h2d_bytes_per_step": sum(h.numel() * 2 for h in host_t), "d2h_bytes_per_step": SCALARS_D2H_BYTES}
+
+    # copy probe: achievable HBM bandwidth in the same process
+    src = torch.empty(1 << 30, dtype=torch.uint8, device="cuda")
+    dst = torch.empty_like(src)
+    for _ in range(3):
+        zb.zg_probe_copy(src, dst, stream)
+    c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    c0.record(stream)
+    for _ in range(10):
+        zb.zg_probe_copy(src, dst, stream)
+    c1.record(stream)
+    torch.cuda.synchronize()
+    probe_gbs = 2 * src.numel() * 10 / (c0.elapsed_time(c1) / 1e3) / 1e9
+    del src, dst
+
+    traffic = recorded_traffic("zg_shard_step", args.workload)
+    out = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": t_max * 1e3 / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic (seeded bf16 gradients, resident in HBM)",
+        "config": {"workload": args.workload, "N": n, "P": p, "loss_scale": ls, "variant": args.variant,
+                   "optimizer": "AdamW lr 1e-3 b 0.9/0.999 eps 1e-8 wd 0.01 clip 1.0",
+                   "l2": f"inputs larger than L2: {(total * 2 * p + n * 14) / 1e9:.2f} GB working set vs 0.129 GB L2, no flush"},
+        "roofline": {"bound": "hbm", "kernel": "zg_shard_step", "achieved": achieved, "peak": peak,
+                     "unit": "GB/s", "frac": achieved / peak, "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
+                     if peak_kind == "measured" else "fallback 6800 GB/s",
+                     "traffic": traffic, "algorithmic_bytes_per_launch": b_step,
+                     "bytes_per_param": accounting.shard_step_bytes_per_param(p)},
+        "kernels": {"zg_grad_norm_us": norm_ms * 1e3, "zg_grad_norm_gbs": b_norm / (norm_ms / 1e3) / 1e9,
+                    "zg_shard_step_us": step_ms * 1e3, "zg_shard_step_gbs": achieved,
+                    "whole_step_gbs": (b_step + b_norm) / (total_ms / K / 1e3) / 1e9,
+                    "probe_copy_gbs": probe_gbs},
+        "e2e": e2e,
+        "gpu_launches": 2 * K,
+        "clocks": clk,
+        "wall_s": wall,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = time_oracle(wl, budget_s=2.0, steps=5)
+    return out if rank == 0 else None
+
+
+# --------------------------------------------------------------------- reference arm
+
+def bench_reference(args) -> dict:
+    from zero_sharded_mixed_flat_gb300 import synth
+
+    wl = synth.workload(args.workload)
+    budget = max(0.01, min(2.0, 120.0 / max(1, args.steps + args.warmup)))
+    cb = time_oracle(wl, budget_s=budget, steps=args.steps, warmup=args.warmup)
+    return {
+        "impl": "reference", "metric": METRIC, "value": cb["value"], "unit": UNIT, "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": cb["seconds"] * 1e3 / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded bf16 gradients)",
+        "config": {"workload": args.workload, "N": wl.n, "P": wl.p, "loss_scale": wl.loss_scale,
+                   "sample": cb["sample"]},
+        "cpu_baseline": {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")},
+        "e2e": {"value": cb["value"], "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None) -> int:
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="flat16m_p8")
+    ap.add_argument("--variant", choices=["ldg", "tma"], default="ldg")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.steps < 1 or args.warmup < 0:
+        ap.error("--steps must be >= 1 and --warmup >= 0")
+    rank, world, local = dist_env()
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(bench_reference(args)), flush=True)
+        return 0
+
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    try:
+        out = bench_ours(args, rank, world, local)
+        if out is not None:
+            print(json.dumps(out), flush=True)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,190 @@
+/*
+ * zg.h -- C ABI of the sharded mixed-precision optimizer step on one GB300.
+ *
+ * What the library computes (ZeRO stage two over a flat parameter vector):
+ * P data-parallel ranks are simulated on one GPU. Each rank r holds a bf16
+ * gradient buffer G_r (already multiplied by the loss scale L) for the whole
+ * flat vector of N parameters. Rank r owns the shard [r*S, min((r+1)*S, N)),
+ * S = zg_shard_len(). For every index i of every shard a step
+ *   1. reduce-scatters: g^_i = G_0[i] + G_1[i] + ... + G_{P-1}[i], in fp32, in
+ *      rank order (Zero From Scratch, item 7: all-reduce is reduce-scatter
+ *      followed by all-gather);
+ *   2. unscales and averages: g_i = g^_i * fp32(1 / (L * P)) (item 6: data
+ *      parallel ranks average their gradients);
+ *   3. takes the global norm over all N: sumsq = sum of fp64(g_i * g_i);
+ *      a non-finite sumsq skips the whole step (nothing is written, the step
+ *      count stays); otherwise c = min(1, max_grad_norm / (norm + norm_eps));
+ *   4. applies AdamW (decoupled weight decay) to the fp32 master weight w_i
+ *      and moments m_i, v_i -- the 4 + 4 + 4 of the sixteen bytes per weight
+ *      of item 1 -- in one fused pass (item 3: one read and one write per
+ *      array instead of one per operation);
+ *   5. writes p_i = bf16(w_i) into the one parameter buffer every rank reads:
+ *      the all-gather.
+ * Per element, every fp32 operation is rounded on its own in the order
+ *   ga = g*c; m = b1*m + (1-b1)*ga; v = b2*v + (1-b2)*(ga*ga);
+ *   mh = m/bc1; vh = v/bc2; d = sqrt(vh) + eps; w = w - (lr*wd)*w;
+ *   w = w - lr*(mh/d); p = bf16_rne(w)
+ * with bc1 = fp32(1 - b1^t), bc2 = fp32(1 - b2^t), b^t kept as fp64 running
+ * products and each constant formed in fp64 and rounded once.
+ * The optional MXFP8 path (item 14) first encodes each rank's gradient per
+ * 32-element block as E4M3 codes plus one E8M0 scale byte, and the step then
+ * sums decoded values instead of bf16 values.
+ *
+ * Citations name a page and a section: "Zero From Scratch" (When the model is
+ * bigger than the machine), its outline items counted from 1 after the
+ * introduction; and the review of the DeepSpeed documentation and tutorials.
+ *
+ * Conventions for every call:
+ *   - Device pointers are plain CUDA device addresses (for example from
+ *     torch), 16-byte aligned, owned by the caller and never freed here.
+ *     A buffer "of n elements" must hold at least n elements; no call reads
+ *     or writes an element at or past n. The shard layout pads each buffer
+ *     to P * S elements; buffers that long are always large enough.
+ *   - A zg_stream is a cudaStream_t (NULL: the legacy default stream). Every
+ *     GPU call is stream-ordered and returns without waiting, except
+ *     zg_get_info and zg_set_step, which synchronise.
+ *   - Return value: ZG_OK (0) or a negative ZG_ERR_* code; nothing else
+ *     crosses the ABI (no exceptions). zg_strerror names a code and
+ *     zg_last_error gives the calling thread's detailed message.
+ *   - One context per stream at a time; contexts are independent.
+ */
+#ifndef ZG_H
+#define ZG_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define ZG_OK 0
+#define ZG_ERR_INVALID_ARG (-1)    /* a size, count, pointer or value out of range */
+#define ZG_ERR_MISALIGNED (-2)     /* a pointer not 16-byte aligned */
+#define ZG_ERR_NOT_BOUND (-3)      /* zg_bind has not been called on this context */
+#define ZG_ERR_CUDA (-4)           /* a CUDA call or launch failed; see zg_last_error */
+#define ZG_ERR_DEVICE_TIMEOUT (-5) /* a bounded device-side wait ran out (status only) */
+#define ZG_ERR_STALE_NORM (-6)     /* a shard step ran without a fresh norm pass (status only) */
+#define ZG_ERR_NO_MEMORY (-7)      /* host or device workspace allocation failed */
+
+#define ZG_MAX_RANKS 16
+
+/* Ways to run the fused step kernel; both compute identical results. */
+#define ZG_VARIANT_LDG 0 /* 128-bit vector loads straight from HBM */
+#define ZG_VARIANT_TMA 1 /* gradient slices staged in shared memory by bulk async copies */
+
+typedef struct CUstream_st *zg_stream; /* same type as cudaStream_t */
+typedef struct zg_ctx zg_ctx;          /* opaque; owned by the library */
+
+typedef struct {
+    double lr, beta1, beta2, eps, weight_decay;
+    double max_grad_norm; /* <= 0 turns the clip off */
+    double norm_eps;      /* added to the norm in the clip ratio, e.g. 1e-6 */
+    int grad_average;     /* 1: average over the P ranks; 0: plain sum */
+} zg_hparams;
+
+typedef struct {
+    double sumsq;     /* global sum of squares of the unscaled, averaged gradient */
+    double norm;      /* sqrt(sumsq) */
+    float clip_coef;  /* c applied in the last step that ran (1 when the clip is off) */
+    int found_inf;    /* 1: the last step saw a non-finite gradient and was skipped */
+    int64_t step_t;   /* applied (not skipped) steps so far */
+    int status;       /* ZG_OK or a device-side ZG_ERR_* code, sticky until zg_get_info */
+} zg_step_info;
+
+/* Create a context for N parameters over P simulated ranks (1 <= P <= 16,
+ * 1 <= N < 2^62) on the current CUDA device. Allocates only a small device
+ * workspace (a few KB: the norm pass's block partials and the step scalars).
+ * Step count starts at 0. Layout: Zero From Scratch, item 17 (one flat
+ * vector cut into P contiguous shards). *out is NULL on failure. */
+int zg_init(int64_t n, int p, const zg_hparams *hp, zg_ctx **out);
+
+/* Shard length S = ceil(N/P) rounded up to a multiple of 32 (one MX block);
+ * rank r owns flat indices [r*S, min((r+1)*S, N)). -1 for a NULL context. */
+int64_t zg_shard_len(const zg_ctx *ctx);
+
+/* Attach the caller's optimizer state: fp32 master weights w, moments m and
+ * v, and the bf16 parameter buffer (each N elements, 16-byte aligned,
+ * device memory). The library keeps the pointers, never the memory. */
+int zg_bind(zg_ctx *ctx, float *w, float *m, float *v, uint16_t *params_bf16);
+
+/* One whole step: zg_grad_norm then zg_shard_step on `stream`.
+ * grad_ptrs: host array of P device pointers, each a bf16 buffer of N
+ * elements (rank r's gradient times loss_scale); read during the call only.
+ * loss_scale: finite and > 0. The skip decision stays on the device. */
+int zg_step(zg_ctx *ctx, const uint16_t *const *grad_ptrs, float loss_scale, zg_stream stream);
+
+/* First half of a step: the global norm (item 7's reduce-scatter, summed and
+ * squared, then one scalar all-reduce, here an ordered sum of block
+ * partials), the found-inf decision, the clip factor and the next bias
+ * corrections, all left in device memory. Reads 2P bytes per parameter. */
+int zg_grad_norm(zg_ctx *ctx, const uint16_t *const *grad_ptrs, float loss_scale, zg_stream stream);
+
+/* Second half: the fused reduce-scatter + unscale + clip + AdamW + bf16
+ * all-gather over every shard, using the decision of the preceding
+ * zg_grad_norm (items 3, 6, 7). Reads 2P + 12 and writes 14 bytes per
+ * parameter. Call exactly once after each zg_grad_norm; a second call finds
+ * the norm consumed, writes nothing and reports ZG_ERR_STALE_NORM in the
+ * status. On a skipped step it writes nothing. */
+int zg_shard_step(zg_ctx *ctx, const uint16_t *const *grad_ptrs, float loss_scale, zg_stream stream);
+
+/* MXFP8-encode one rank's bf16 buffer of n elements (Zero From Scratch,
+ * item 14): per block k of 32 elements [32k, 32k+32), amax = max |x|;
+ * e = floor(log2 amax) - 8 clamped to [-127, 127] (e = -127 for an all-zero
+ * block); scales[k] = e + 127 (E8M0); codes[i] = E4M3(x_i * 2^-e), round to
+ * nearest even, magnitudes at or above 448 saturate to 448, signs kept.
+ * A block holding an infinity or NaN gets scale 0xFF and codes 0x7F (NaN).
+ * Elements past n count as zero in the last block's amax and get no code.
+ * codes: n bytes; scales: ceil(n/32) bytes; both device memory. n >= 0. */
+int zg_quant_mxfp8(const uint16_t *in, int64_t n, uint8_t *codes, uint8_t *scales, zg_stream stream);
+
+/* Whole step from MX-encoded gradients: codes[r] (N bytes) and scales[r]
+ * (ceil(N/32) bytes) are rank r's zg_quant_mxfp8 output for its N-element
+ * buffer. Each rank value is decoded as E4M3(code) * 2^(scale - 127) before
+ * the rank-ordered sum; the rest is zg_step. */
+int zg_step_mxfp8(zg_ctx *ctx, const uint8_t *const *codes, const uint8_t *const *scales,
+                  float loss_scale, zg_stream stream);
+
+/* The two halves of zg_step_mxfp8, for separate timing. */
+int zg_grad_norm_mxfp8(zg_ctx *ctx, const uint8_t *const *codes, const uint8_t *const *scales,
+                       float loss_scale, zg_stream stream);
+int zg_shard_step_mxfp8(zg_ctx *ctx, const uint8_t *const *codes, const uint8_t *const *scales,
+                        float loss_scale, zg_stream stream);
+
+/* Wait for `stream`, then copy out the step scalars. Reports and clears the
+ * sticky device status. This is the only device-to-host read of a step. */
+int zg_get_info(zg_ctx *ctx, zg_stream stream, zg_step_info *info);
+
+/* Resume: set the applied-step count to t >= 0; the running powers b1^t and
+ * b2^t are rebuilt by t multiplications from 1, as an uninterrupted run forms
+ * them, so steps after a resume match an uninterrupted run bit for bit.
+ * Synchronises the device; no step may be in flight on this context. */
+int zg_set_step(zg_ctx *ctx, int64_t t);
+
+/* Choose the fused step kernel (ZG_VARIANT_LDG or ZG_VARIANT_TMA). */
+int zg_set_variant(zg_ctx *ctx, int variant);
+
+/* Bound, in polls, on each device-side wait of the TMA variant (default a
+ * few million, far above any healthy wait). A wait that runs out makes the
+ * kernel drain its own copies, skip its remaining work and record
+ * ZG_ERR_DEVICE_TIMEOUT in the status. 0 makes every first poll run out
+ * (used to test that path). */
+int zg_set_wait_limit(zg_ctx *ctx, int64_t polls);
+
+/* Measurement aid: copy `bytes` (a multiple of 16, both pointers 16-byte
+ * aligned device memory) with a plain streaming copy kernel; its time gives
+ * the achievable HBM bandwidth in the same run. */
+int zg_probe_copy(const void *src, void *dst, int64_t bytes, zg_stream stream);
+
+/* Free the context and its workspace (after the stream work using it is done). */
+void zg_destroy(zg_ctx *ctx);
+
+const char *zg_strerror(int code);
+const char *zg_last_error(void); /* this thread's last detailed message */
+int zg_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ZG_H */

@@ -1,0 +1,69 @@
+"""The C-ABI library without a GPU: it builds, loads, exports every function
+include/zg.h declares, and rejects bad arguments before touching CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from zero_sharded_mixed_flat_gb300 import binding as zb
+from zero_sharded_mixed_flat_gb300 import build as zbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    zbuild.build()
+    return zb.lib()
+
+
+def declared_functions() -> list[str]:
+    text = open(os.path.join(ROOT, "include", "zg.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(zg_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 19
+    for name in names:
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for code in range(0, -8, -1):
+        assert lib.zg_strerror(code)
+    assert lib.zg_strerror(-99) == b"unknown status"
+    assert lib.zg_version() >= 100
+
+
+def test_host_side_validation_needs_no_gpu(lib):
+    hp = zb._Hp(1e-3, 0.9, 0.999, 1e-8, 0.01, 1.0, 1e-6, 1)
+    out = ctypes.c_void_p()
+    for n, p in ((0, 4), (-1, 4), (1 << 62, 4), (10, 0), (10, 17)):
+        assert lib.zg_init(n, p, ctypes.byref(hp), ctypes.byref(out)) == zb.ZG_ERR_INVALID_ARG
+        assert out.value is None
+    for field, bad in (("beta1", 1.0), ("beta2", -0.1), ("lr", float("nan")), ("eps", -1.0), ("grad_average", 2)):
+        h = zb._Hp(1e-3, 0.9, 0.999, 1e-8, 0.01, 1.0, 1e-6, 1)
+        setattr(h, field, bad)
+        assert lib.zg_init(10, 2, ctypes.byref(h), ctypes.byref(out)) == zb.ZG_ERR_INVALID_ARG
+    assert lib.zg_init(10, 2, None, ctypes.byref(out)) == zb.ZG_ERR_INVALID_ARG
+    assert lib.zg_shard_len(None) == -1
+    assert lib.zg_step(None, None, 1.0, None) == zb.ZG_ERR_INVALID_ARG
+    assert lib.zg_get_info(None, None, None) == zb.ZG_ERR_INVALID_ARG
+    assert lib.zg_quant_mxfp8(None, -1, None, None, None) == zb.ZG_ERR_INVALID_ARG
+    assert lib.zg_quant_mxfp8(None, 0, None, None, None) == zb.ZG_OK  # nothing to do
+    assert lib.zg_probe_copy(None, None, 15, None) == zb.ZG_ERR_INVALID_ARG
+    assert b"multiple of 16" in lib.zg_last_error()
+    lib.zg_destroy(None)
+
+
+def test_no_cpu_fallback_without_a_gpu(lib):
+    import torch
+
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    with pytest.raises(zb.ZgError) as e:
+        zb.zg_init(1024, 4)
+    assert e.value.code == zb.ZG_ERR_CUDA

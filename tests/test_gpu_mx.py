@@ -1,0 +1,98 @@
+"""The MXFP8 path on the GPU vs the oracle: codes and scale bytes bit-exact,
+and the step from decoded codes within the step tolerances
+(Zero From Scratch, item 14: E4M3 elements, one power-of-two scale per 32)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_helpers import Guarded, log, to_dev_bf16
+from test_gpu_step import GpuRun, check_step
+from zero_sharded_mixed_flat_gb300 import binding as zb
+from zero_sharded_mixed_flat_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+
+def gpu_encode(x: np.ndarray):
+    n = x.size
+    codes = Guarded(n, torch.uint8)
+    scales = Guarded((n + 31) // 32, torch.uint8)
+    zb.zg_quant_mxfp8(to_dev_bf16(x), codes.view, scales.view, n)
+    torch.cuda.synchronize()
+    assert codes.intact() and scales.intact()
+    return codes.view.cpu().numpy(), scales.view.cpu().numpy()
+
+
+def special_blocks() -> np.ndarray:
+    """Hand-made blocks: zeros and negative zeros, bf16 subnormals, amax at
+    448 * 2^k and just below 512 * 2^k, ties between E4M3 neighbours, huge
+    and tiny magnitudes, and blocks poisoned by inf or NaN."""
+    f = lambda vals: (np.array(vals, dtype=np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    blocks = [np.zeros(32, np.uint16), np.full(32, 0x8000, np.uint16), np.arange(32, dtype=np.uint16)]
+    for k in (-130, -20, 0, 7, 100, 119):
+        b = np.zeros(32, np.float32)
+        b[0] = 448.0 * 2.0 ** k if k > -126 else 2.0 ** -126
+        b[1:] = np.linspace(-1, 1, 31) * 2.0 ** k
+        blocks.append(f(b))
+        blocks.append(f(np.full(32, 510.0 * 2.0 ** min(k, 119))))
+    tie = np.zeros(32, np.float32)
+    tie[0] = 1.0
+    tie[1:9] = [2.0 ** -17, 2.0 ** -18, 3 * 2.0 ** -19, -(2.0 ** -20), 1.0625, 1.1875, -1.0625, 17.0 / 16]
+    blocks.append(f(tie))
+    for bad in (0x7F80, 0xFF80, 0x7FC0, 0xFFC1):
+        b = f(np.linspace(-3, 3, 32))
+        b[13] = bad
+        blocks.append(b)
+    return np.concatenate(blocks)
+
+
+@pytest.mark.parametrize("tail", [0, 1, 8, 13, 31])
+def test_quant_bit_exact(tail):
+    parts = [special_blocks(),
+             np.arange(65536, dtype=np.uint32).astype(np.uint16),  # every bf16 pattern
+             np.random.default_rng(2).permutation(np.arange(65536, dtype=np.uint32).astype(np.uint16)),
+             synth.random_bf16(32 * 4000, seed=1, scale=1e-3, dist="student_t"),
+             synth.random_bf16(32 * 4000, seed=2, scale=1.0, dist="logspread")]
+    x = np.concatenate(parts)
+    x = x[: (x.size // 32) * 32 - (32 - tail) % 32] if tail else x[: (x.size // 32) * 32]
+    gc, gs = gpu_encode(x)
+    rc, rs = oracle.mx_encode(x)
+    bad_c = np.nonzero(gc != rc)[0]
+    bad_s = np.nonzero(gs != rs)[0]
+    log({"case": f"mx-quant tail={tail}", "n": int(x.size), "code_mismatch": int(bad_c.size),
+         "scale_mismatch": int(bad_s.size)})
+    assert bad_s.size == 0, [(int(i), int(gs[i]), int(rs[i])) for i in bad_s[:8]]
+    assert bad_c.size == 0, [(int(i), hex(x[i]), int(gc[i]), int(rc[i])) for i in bad_c[:8]]
+
+
+def test_quant_empty_and_tiny():
+    for n in (1, 2, 31, 33):
+        x = synth.random_bf16(n, seed=n, scale=3.0)
+        gc, gs = gpu_encode(x)
+        rc, rs = oracle.mx_encode(x)
+        assert np.array_equal(gc, rc) and np.array_equal(gs, rs)
+    zb.zg_quant_mxfp8(torch.zeros(8, dtype=torch.bfloat16, device="cuda"),
+                      torch.zeros(8, dtype=torch.uint8, device="cuda"),
+                      torch.zeros(1, dtype=torch.uint8, device="cuda"), n=0)
+
+
+@pytest.mark.parametrize("n,p", [(1, 1), (33, 2), (1000, 3), (65_549, 8), (4096, 16)])
+def test_mx_step_small(n, p):
+    rng = np.random.default_rng(n + p)
+    w0 = (rng.standard_normal(n) * 0.02).astype(np.float32)
+    run = GpuRun(w0, p)
+    ref = oracle.OracleOptimizer(w0)
+    for k in range(4):
+        host = [synth.random_bf16(n, seed=500 + 10 * k + r, scale=1e-3 if k != 1 else 1.0, dist="student_t")
+                for r in range(p)]
+        if k == 2:
+            host[p - 1][n - 1] = 0x7F80
+        enc = [oracle.mx_encode(h) for h in host]
+        codes = [torch.from_numpy(c).cuda() for c, _ in enc]
+        scales = [torch.from_numpy(s).cuda() for _, s in enc]
+        zb.zg_step_mxfp8(run.ctx, codes, scales, 1.0)
+        info = zb.zg_get_info(run.ctx)
+        dec = ref.step_mx([c for c, _ in enc], [s for _, s in enc], 1.0)
+        check_step(f"mx-step n={n} p={p}", run, ref, dec, info, k + 1)
+    assert ref.t == 3

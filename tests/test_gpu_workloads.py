@@ -1,0 +1,95 @@
+"""The GPU step vs the oracle on the full workloads, every step, every element.
+
+  flat65k_p4     N = 65,536, P = 4, 10 steps
+  flat16m_p8     N = 2^24, P = 8, 20 steps, +inf on rank 3 at step 7 (skipped)
+  gpt2small_p8   N = 124,439,808, P = 8, per-tensor scales, loss scale 65,536, 5 steps
+  mxfp8_128m_p8  N = 2^27, P = 8, Student-t grads encoded to MXFP8 on the GPU
+                 (codes and scales bit-exact vs the oracle's encoder), 5 steps
+
+Tolerances: w, m, v relative 2e-6 per step and 1e-5 after ten; bf16 params
+one ulp; norm 1e-5; skip decisions exact; MX codes and scales exact.
+"""
+from concurrent.futures import ThreadPoolExecutor
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_helpers import compare_state, log, to_dev_bf16, to_host_f32, to_host_u16
+from zero_sharded_mixed_flat_gb300 import binding as zb
+from zero_sharded_mixed_flat_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+
+def _gpu_state(opt: zb.ShardedAdamW) -> dict:
+    return {"w": to_host_f32(opt.w), "m": to_host_f32(opt.m), "v": to_host_f32(opt.v), "p": to_host_u16(opt.params)}
+
+
+def _check(tag, opt, ref, dec, info, k):
+    assert info.status == 0
+    assert info.found_inf == dec.found_inf, (tag, k)
+    assert info.step_t == ref.t, (tag, k, info.step_t, ref.t)
+    if not dec.found_inf:
+        assert abs(info.norm - dec.norm) <= 1e-5 * dec.norm, (tag, k, info.norm, dec.norm)
+    st = compare_state(f"{tag}/step{k}", _gpu_state(opt), {"w": ref.w, "m": ref.m, "v": ref.v, "p": ref.p},
+                       min(1e-5, 2e-6 * max(ref.t, 1)))
+    st.update(norm_gpu=info.norm, norm_ref=dec.norm, clip_gpu=info.clip_coef, clip_ref=dec.clip,
+              found_inf=dec.found_inf)
+    log(st)
+    if info.clip_coef == dec.clip:
+        assert st["w_bitexact"] == st["m_bitexact"] == st["v_bitexact"] == st["p_bitexact"] == 1.0, st
+    return st
+
+
+@pytest.mark.parametrize("name", ["flat65k_p4", "flat16m_p8", "gpt2small_p8"])
+def test_bf16_workload(name):
+    w = synth.workload(name)
+    total = synth.padded_len(w)
+    w0 = synth.init_weights(w)
+    opt = zb.ShardedAdamW(w.n, w.p, zb.Hparams(), torch.from_numpy(w0))
+    assert opt.shard_len * w.p == total
+    ref = oracle.OracleOptimizer(w0)
+    dev = [torch.empty(total, dtype=torch.bfloat16, device="cuda") for _ in range(w.p)]
+    skipped = []
+    for k in range(1, w.steps + 1):
+        host = synth.step_grads(w, k)
+        for r in range(w.p):
+            to_dev_bf16(host[r], dev[r])
+        opt.step(dev, w.loss_scale)
+        info = opt.info()
+        dec = ref.step(host, w.loss_scale)
+        _check(name, opt, ref, dec, info, k)
+        if dec.found_inf:
+            skipped.append(k)
+    assert skipped == ([w.inf_step] if w.inf_step else [])
+    assert ref.t == w.steps - len(skipped)
+
+
+def test_mxfp8_workload():
+    w = synth.workload("mxfp8_128m_p8")
+    n, p = w.n, w.p
+    nb = (n + 31) // 32
+    w0 = synth.init_weights(w)
+    opt = zb.ShardedAdamW(n, p, zb.Hparams(), torch.from_numpy(w0))
+    ref = oracle.OracleOptimizer(w0)
+    xdev = torch.empty(n, dtype=torch.bfloat16, device="cuda")
+    codes = [torch.empty(n, dtype=torch.uint8, device="cuda") for _ in range(p)]
+    scales = [torch.empty(nb, dtype=torch.uint8, device="cuda") for _ in range(p)]
+    with ThreadPoolExecutor(p) as pool:
+        for k in range(1, w.steps + 1):
+            host = [synth.grads_bf16(w, k, r) for r in range(p)]
+            ref_enc = list(pool.map(oracle.mx_encode, host))
+            for r in range(p):
+                to_dev_bf16(host[r], xdev)
+                zb.zg_quant_mxfp8(xdev, codes[r], scales[r], n)
+                gc, gs = codes[r].cpu().numpy(), scales[r].cpu().numpy()
+                assert np.array_equal(gs, ref_enc[r][1]), (k, r, int(np.sum(gs != ref_enc[r][1])))
+                assert np.array_equal(gc, ref_enc[r][0]), (k, r, int(np.sum(gc != ref_enc[r][0])))
+            log({"case": f"mxfp8_128m_p8/step{k}/encode", "codes_bitexact": 1.0, "scales_bitexact": 1.0})
+            opt.step_mxfp8(codes, scales, w.loss_scale)
+            info = opt.info()
+            dec = ref.step_mx([c for c, _ in ref_enc], [s for _, s in ref_enc], w.loss_scale)
+            _check("mxfp8_128m_p8", opt, ref, dec, info, k)
+    assert ref.t == w.steps

@@ -1,0 +1,351 @@
+// zg_api.cu -- the C ABI declared in include/zg.h: argument checks, the
+// small device workspace, and the launches. No kernel runs on the host and
+// no call here allocates anything per step.
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdarg.h>
+#include <stdint.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <map>
+#include <mutex>
+#include <utility>
+
+#include "zg.h"
+#include "zg_launch.h"
+
+struct zg_ctx {
+    int64_t n;
+    int p;
+    int64_t s;
+    zg_hparams hp;
+    zg::FinalizeK fk;
+    zg::StepK k;
+    float *w, *m, *v;
+    uint16_t *params;
+    bool bound;
+    int device;
+    zg::Scalars *d_sc;
+    double *d_partials;
+    int partials_cap;
+    zg::Scalars *h_sc;
+    int variant;
+    long long wait_limit;
+};
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+int fail(int code, const char *fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof g_err, fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+int cuda_fail(cudaError_t e, const char *what)
+{
+    return fail(ZG_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorString(e), cudaGetErrorName(e));
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+constexpr int kPartialsCap = 8192;
+constexpr long long kDefaultWaitLimit = 4000000;
+
+int check_ctx(const zg_ctx *ctx, bool need_bound)
+{
+    if (!ctx) return fail(ZG_ERR_INVALID_ARG, "context is NULL");
+    if (need_bound && !ctx->bound) return fail(ZG_ERR_NOT_BOUND, "zg_bind has not been called");
+    return ZG_OK;
+}
+
+int check_scale(float loss_scale)
+{
+    if (!(loss_scale > 0.0f) || !isfinite(loss_scale))
+        return fail(ZG_ERR_INVALID_ARG, "loss_scale must be finite and > 0 (got %g)", double(loss_scale));
+    return ZG_OK;
+}
+
+template <class T>
+int check_rank_ptrs(const zg_ctx *ctx, const T *const *ptrs, const char *what, bool need_align)
+{
+    if (!ptrs) return fail(ZG_ERR_INVALID_ARG, "%s array is NULL", what);
+    for (int r = 0; r < ctx->p; ++r) {
+        if (!ptrs[r]) return fail(ZG_ERR_INVALID_ARG, "%s[%d] is NULL", what, r);
+        if (need_align && !aligned16(ptrs[r])) return fail(ZG_ERR_MISALIGNED, "%s[%d] is not 16-byte aligned", what, r);
+    }
+    return ZG_OK;
+}
+
+float inv_scale(const zg_ctx *ctx, float loss_scale)
+{
+    const double denom = double(loss_scale) * (ctx->hp.grad_average ? double(ctx->p) : 1.0);
+    return float(1.0 / denom);
+}
+
+zg::State state_of(const zg_ctx *ctx) { return zg::State{ctx->w, ctx->m, ctx->v, ctx->params}; }
+
+int finish_launch(cudaError_t e, const char *what) { return e == cudaSuccess ? ZG_OK : cuda_fail(e, what); }
+
+}  // namespace
+
+namespace zg {
+
+int wave_blocks(const void *kernel, int threads, size_t smem)
+{
+    static std::mutex mu;
+    static std::map<std::pair<int, const void *>, int> cache;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    std::lock_guard<std::mutex> lock(mu);
+    auto key = std::make_pair(dev, kernel);
+    auto it = cache.find(key);
+    if (it != cache.end()) return it->second;
+    int sms = 0, per_sm = 0;
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem);
+    int blocks = sms * per_sm;
+    if (blocks < 1) blocks = 1;
+    cache[key] = blocks;
+    return blocks;
+}
+
+int norm_blocks_cap() { return kPartialsCap; }
+
+}  // namespace zg
+
+extern "C" {
+
+int zg_version(void) { return 100; }
+
+const char *zg_last_error(void) { return g_err; }
+
+const char *zg_strerror(int code)
+{
+    switch (code) {
+    case ZG_OK: return "ok";
+    case ZG_ERR_INVALID_ARG: return "invalid argument";
+    case ZG_ERR_MISALIGNED: return "pointer not 16-byte aligned";
+    case ZG_ERR_NOT_BOUND: return "optimizer state not bound (call zg_bind)";
+    case ZG_ERR_CUDA: return "CUDA error";
+    case ZG_ERR_DEVICE_TIMEOUT: return "a bounded device-side wait ran out";
+    case ZG_ERR_STALE_NORM: return "shard step without a fresh norm pass";
+    case ZG_ERR_NO_MEMORY: return "out of memory";
+    default: return "unknown status";
+    }
+}
+
+int zg_init(int64_t n, int p, const zg_hparams *hp, zg_ctx **out)
+{
+    if (!out) return fail(ZG_ERR_INVALID_ARG, "out is NULL");
+    *out = nullptr;
+    if (n < 1 || n >= (int64_t(1) << 62)) return fail(ZG_ERR_INVALID_ARG, "N must be in [1, 2^62) (got %lld)", (long long)n);
+    if (p < 1 || p > ZG_MAX_RANKS) return fail(ZG_ERR_INVALID_ARG, "P must be in [1, %d] (got %d)", ZG_MAX_RANKS, p);
+    if (!hp) return fail(ZG_ERR_INVALID_ARG, "hparams is NULL");
+    const double vals[] = {hp->lr, hp->beta1, hp->beta2, hp->eps, hp->weight_decay, hp->max_grad_norm, hp->norm_eps};
+    for (double x : vals)
+        if (!isfinite(x)) return fail(ZG_ERR_INVALID_ARG, "hyperparameters must be finite");
+    if (hp->lr < 0 || hp->eps < 0 || hp->norm_eps < 0) return fail(ZG_ERR_INVALID_ARG, "lr, eps and norm_eps must be >= 0");
+    if (!(hp->beta1 >= 0 && hp->beta1 < 1 && hp->beta2 >= 0 && hp->beta2 < 1))
+        return fail(ZG_ERR_INVALID_ARG, "betas must be in [0, 1)");
+    if (hp->grad_average != 0 && hp->grad_average != 1) return fail(ZG_ERR_INVALID_ARG, "grad_average must be 0 or 1");
+
+    zg_ctx *ctx = new (std::nothrow) zg_ctx();
+    if (!ctx) return fail(ZG_ERR_NO_MEMORY, "host allocation of the context failed");
+    ctx->n = n;
+    ctx->p = p;
+    int64_t s = (n + p - 1) / p;
+    ctx->s = (s + 31) / 32 * 32;
+    ctx->hp = *hp;
+    ctx->fk = zg::FinalizeK{hp->beta1, hp->beta2, hp->max_grad_norm, hp->norm_eps};
+    ctx->k = zg::StepK{float(hp->beta1),       float(hp->beta2), float(1.0 - hp->beta1), float(1.0 - hp->beta2),
+                       float(hp->eps),         float(hp->lr),    float(hp->lr * hp->weight_decay)};
+    ctx->variant = ZG_VARIANT_LDG;
+    ctx->wait_limit = kDefaultWaitLimit;
+    ctx->partials_cap = zg::norm_blocks_cap();
+    cudaError_t e = cudaGetDevice(&ctx->device);
+    if (e == cudaSuccess) e = cudaMalloc(&ctx->d_sc, sizeof(zg::Scalars));
+    if (e == cudaSuccess) e = cudaMalloc(&ctx->d_partials, sizeof(double) * ctx->partials_cap);
+    if (e == cudaSuccess) e = cudaMallocHost(&ctx->h_sc, sizeof(zg::Scalars));
+    if (e == cudaSuccess) {
+        memset(ctx->h_sc, 0, sizeof(zg::Scalars));
+        ctx->h_sc->b1p = 1.0;
+        ctx->h_sc->b2p = 1.0;
+        ctx->h_sc->clip = 1.0f;
+        e = cudaMemcpy(ctx->d_sc, ctx->h_sc, sizeof(zg::Scalars), cudaMemcpyHostToDevice);
+    }
+    if (e != cudaSuccess) {
+        int rc = cuda_fail(e, "zg_init workspace");
+        cudaGetLastError();
+        zg_destroy(ctx);
+        return rc;
+    }
+    *out = ctx;
+    return ZG_OK;
+}
+
+int64_t zg_shard_len(const zg_ctx *ctx) { return ctx ? ctx->s : -1; }
+
+int zg_bind(zg_ctx *ctx, float *w, float *m, float *v, uint16_t *params_bf16)
+{
+    if (int rc = check_ctx(ctx, false)) return rc;
+    if (!w || !m || !v || !params_bf16) return fail(ZG_ERR_INVALID_ARG, "state pointers must not be NULL");
+    if (!aligned16(w) || !aligned16(m) || !aligned16(v) || !aligned16(params_bf16))
+        return fail(ZG_ERR_MISALIGNED, "state pointers must be 16-byte aligned");
+    ctx->w = w;
+    ctx->m = m;
+    ctx->v = v;
+    ctx->params = params_bf16;
+    ctx->bound = true;
+    return ZG_OK;
+}
+
+int zg_grad_norm(zg_ctx *ctx, const uint16_t *const *grad_ptrs, float loss_scale, zg_stream stream)
+{
+    if (int rc = check_ctx(ctx, false)) return rc;
+    if (int rc = check_scale(loss_scale)) return rc;
+    if (int rc = check_rank_ptrs(ctx, grad_ptrs, "grad_ptrs", true)) return rc;
+    return finish_launch(zg::launch_norm_bf16(ctx->p, grad_ptrs, ctx->n, inv_scale(ctx, loss_scale), ctx->d_partials,
+                                              ctx->partials_cap, ctx->d_sc, ctx->fk, stream),
+                         "norm pass launch");
+}
+
+int zg_shard_step(zg_ctx *ctx, const uint16_t *const *grad_ptrs, float loss_scale, zg_stream stream)
+{
+    if (int rc = check_ctx(ctx, true)) return rc;
+    if (int rc = check_scale(loss_scale)) return rc;
+    if (int rc = check_rank_ptrs(ctx, grad_ptrs, "grad_ptrs", true)) return rc;
+    return finish_launch(zg::launch_step_bf16(ctx->p, grad_ptrs, ctx->n, inv_scale(ctx, loss_scale), ctx->k,
+                                              state_of(ctx), ctx->d_sc, stream),
+                         "step pass launch");
+}
+
+int zg_step(zg_ctx *ctx, const uint16_t *const *grad_ptrs, float loss_scale, zg_stream stream)
+{
+    if (int rc = check_ctx(ctx, true)) return rc;
+    if (int rc = zg_grad_norm(ctx, grad_ptrs, loss_scale, stream)) return rc;
+    return zg_shard_step(ctx, grad_ptrs, loss_scale, stream);
+}
+
+int zg_quant_mxfp8(const uint16_t *in, int64_t n, uint8_t *codes, uint8_t *scales, zg_stream stream)
+{
+    if (n < 0 || n >= (int64_t(1) << 62)) return fail(ZG_ERR_INVALID_ARG, "n must be in [0, 2^62)");
+    if (n == 0) return ZG_OK;
+    if (!in || !codes || !scales) return fail(ZG_ERR_INVALID_ARG, "pointers must not be NULL");
+    if (!aligned16(in) || !aligned16(codes)) return fail(ZG_ERR_MISALIGNED, "in and codes must be 16-byte aligned");
+    return finish_launch(zg::launch_quant(in, n, codes, scales, stream), "MXFP8 encoder launch");
+}
+
+int zg_grad_norm_mxfp8(zg_ctx *ctx, const uint8_t *const *codes, const uint8_t *const *scales, float loss_scale,
+                       zg_stream stream)
+{
+    if (int rc = check_ctx(ctx, false)) return rc;
+    if (int rc = check_scale(loss_scale)) return rc;
+    if (int rc = check_rank_ptrs(ctx, codes, "codes", true)) return rc;
+    if (int rc = check_rank_ptrs(ctx, scales, "scales", false)) return rc;
+    return finish_launch(zg::launch_norm_mx(ctx->p, codes, scales, ctx->n, inv_scale(ctx, loss_scale), ctx->d_partials,
+                                            ctx->partials_cap, ctx->d_sc, ctx->fk, stream),
+                         "MX norm pass launch");
+}
+
+int zg_shard_step_mxfp8(zg_ctx *ctx, const uint8_t *const *codes, const uint8_t *const *scales, float loss_scale,
+                        zg_stream stream)
+{
+    if (int rc = check_ctx(ctx, true)) return rc;
+    if (int rc = check_scale(loss_scale)) return rc;
+    if (int rc = check_rank_ptrs(ctx, codes, "codes", true)) return rc;
+    if (int rc = check_rank_ptrs(ctx, scales, "scales", false)) return rc;
+    return finish_launch(zg::launch_step_mx(ctx->p, codes, scales, ctx->n, inv_scale(ctx, loss_scale), ctx->k,
+                                            state_of(ctx), ctx->d_sc, stream),
+                         "MX step pass launch");
+}
+
+int zg_step_mxfp8(zg_ctx *ctx, const uint8_t *const *codes, const uint8_t *const *scales, float loss_scale,
+                  zg_stream stream)
+{
+    if (int rc = check_ctx(ctx, true)) return rc;
+    if (int rc = zg_grad_norm_mxfp8(ctx, codes, scales, loss_scale, stream)) return rc;
+    return zg_shard_step_mxfp8(ctx, codes, scales, loss_scale, stream);
+}
+
+int zg_get_info(zg_ctx *ctx, zg_stream stream, zg_step_info *info)
+{
+    if (int rc = check_ctx(ctx, false)) return rc;
+    if (!info) return fail(ZG_ERR_INVALID_ARG, "info is NULL");
+    cudaError_t e = cudaMemcpyAsync(ctx->h_sc, ctx->d_sc, sizeof(zg::Scalars), cudaMemcpyDeviceToHost, stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return cuda_fail(e, "zg_get_info");
+    const zg::Scalars &h = *ctx->h_sc;
+    info->sumsq = h.sumsq;
+    info->norm = h.norm;
+    info->clip_coef = h.clip;
+    info->found_inf = h.found_inf;
+    info->step_t = h.t;
+    info->status = h.status;
+    if (h.status != 0) {
+        e = cudaMemsetAsync(reinterpret_cast<char *>(ctx->d_sc) + offsetof(zg::Scalars, status), 0, sizeof(int), stream);
+        if (e != cudaSuccess) return cuda_fail(e, "zg_get_info status reset");
+    }
+    return ZG_OK;
+}
+
+int zg_set_step(zg_ctx *ctx, int64_t t)
+{
+    if (int rc = check_ctx(ctx, false)) return rc;
+    if (t < 0) return fail(ZG_ERR_INVALID_ARG, "t must be >= 0");
+    double b1p = 1.0, b2p = 1.0;
+    for (int64_t i = 0; i < t; ++i) {
+        b1p = b1p * ctx->hp.beta1;
+        b2p = b2p * ctx->hp.beta2;
+    }
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e == cudaSuccess) e = cudaMemcpy(ctx->h_sc, ctx->d_sc, sizeof(zg::Scalars), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "zg_set_step read");
+    ctx->h_sc->t = t;
+    ctx->h_sc->b1p = b1p;
+    ctx->h_sc->b2p = b2p;
+    ctx->h_sc->step_gen = ctx->h_sc->norm_gen;  // any pending norm predates the resume
+    e = cudaMemcpy(ctx->d_sc, ctx->h_sc, sizeof(zg::Scalars), cudaMemcpyHostToDevice);
+    return e == cudaSuccess ? ZG_OK : cuda_fail(e, "zg_set_step write");
+}
+
+int zg_set_variant(zg_ctx *ctx, int variant)
+{
+    if (int rc = check_ctx(ctx, false)) return rc;
+    if (variant != ZG_VARIANT_LDG) return fail(ZG_ERR_INVALID_ARG, "unknown or unavailable variant %d", variant);
+    ctx->variant = variant;
+    return ZG_OK;
+}
+
+int zg_set_wait_limit(zg_ctx *ctx, int64_t polls)
+{
+    if (int rc = check_ctx(ctx, false)) return rc;
+    if (polls < 0) return fail(ZG_ERR_INVALID_ARG, "polls must be >= 0");
+    ctx->wait_limit = polls;
+    return ZG_OK;
+}
+
+int zg_probe_copy(const void *src, void *dst, int64_t bytes, zg_stream stream)
+{
+    if (bytes < 0 || bytes % 16) return fail(ZG_ERR_INVALID_ARG, "bytes must be a non-negative multiple of 16");
+    if (bytes == 0) return ZG_OK;
+    if (!src || !dst) return fail(ZG_ERR_INVALID_ARG, "pointers must not be NULL");
+    if (!aligned16(src) || !aligned16(dst)) return fail(ZG_ERR_MISALIGNED, "pointers must be 16-byte aligned");
+    return finish_launch(zg::launch_copy(src, dst, bytes, stream), "copy probe launch");
+}
+
+void zg_destroy(zg_ctx *ctx)
+{
+    if (!ctx) return;
+    if (ctx->d_sc) cudaFree(ctx->d_sc);
+    if (ctx->d_partials) cudaFree(ctx->d_partials);
+    if (ctx->h_sc) cudaFreeHost(ctx->h_sc);
+    delete ctx;
+}
+
+}  // extern "C"

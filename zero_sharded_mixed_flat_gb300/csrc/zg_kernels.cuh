@@ -1,0 +1,476 @@
+// zg_kernels.cuh -- device code of the sharded mixed-precision optimizer step.
+//
+// Memory-bound throughout (about 20 fp32 operations against 2P + 26 bytes
+// per parameter), so no tensor cores: the design goal is one coalesced
+// 128-bit read and write per array per element and enough bytes in flight
+// per SM to keep HBM3e busy.
+//
+// Numerics: every per-element operation uses a correctly rounded intrinsic
+// (__fadd_rn, __fmul_rn, __fdiv_rn, __fsqrt_rn), which the compiler never
+// fuses into an FMA, in the order the step is defined:
+//   g  = (G_0 + G_1 + ... + G_{P-1}) * inv        (reduce-scatter + unscale)
+//   ga = g * c; m = b1*m + (1-b1)*ga; v = b2*v + (1-b2)*(ga*ga)
+//   mh = m/bc1; vh = v/bc2; d = sqrt(vh) + eps
+//   w = w - (lr*wd)*w; w = w - lr*(mh/d); p = bf16_rne(w)
+// (Zero From Scratch, items 3, 6 and 7; the AdamW form is the textbook one
+// with decoupled weight decay, the pages print no formula.)
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <type_traits>
+
+namespace zg {
+
+constexpr int kMaxRanks = 16;
+constexpr int kVec = 8;  // elements per thread per iteration: one 16-byte bf16 load
+
+// Device-resident step scalars. The norm pass writes the "pending" decision;
+// the step pass consumes it and commits the step count. The host reads the
+// block only in zg_get_info, so a skipped step never needs a host round trip.
+struct Scalars {
+    double sumsq;
+    double norm;
+    double b1p_next;
+    double b2p_next;
+    int64_t t_next;
+    float clip;
+    float bc1;
+    float bc2;
+    int found_inf;
+    int64_t t;
+    double b1p;
+    double b2p;
+    unsigned int norm_ticket;  // norm-pass blocks finished in the current launch
+    unsigned int step_ticket;  // step-pass blocks finished in the current launch
+    unsigned int norm_gen;     // bumped by every norm finalize
+    unsigned int step_gen;     // = norm_gen once a step pass consumed that norm
+    int status;                // sticky device status (ZG_OK or ZG_ERR_*)
+    int pad_;
+};
+
+struct FinalizeK {
+    double beta1, beta2, max_grad_norm, norm_eps;
+};
+
+// Per-step fp32 constants, each formed in fp64 on the host and rounded once.
+struct StepK {
+    float b1, b2, omb1, omb2, eps, lr, lrwd;
+};
+
+struct State {
+    float *w, *m, *v;
+    uint16_t *p;
+};
+
+constexpr int kStatusTimeout = -5;     // ZG_ERR_DEVICE_TIMEOUT
+constexpr int kStatusStaleNorm = -6;   // ZG_ERR_STALE_NORM
+
+// ------------------------------------------------------------------ loads
+
+__device__ __forceinline__ uint4 ld_stream(const uint4 *p) { return __ldcs(p); }
+__device__ __forceinline__ uint2 ld_stream(const uint2 *p) { return __ldcs(p); }
+__device__ __forceinline__ float4 ld_stream(const float4 *p) { return __ldcs(p); }
+__device__ __forceinline__ void st_stream(float4 *p, float4 v) { __stcs(p, v); }
+__device__ __forceinline__ void st_stream(uint4 *p, uint4 v) { __stcs(p, v); }
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// Two binary32 values to packed bf16 (lo in bits 0..15), round to nearest even.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
+{
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+// ------------------------------------------------------------------ MXFP8
+
+// E8M0 scale byte to its value 2^(s - 127) as a binary32; 0 gives the
+// subnormal 2^-127 and 0xFF is NaN.
+__device__ __forceinline__ float e8m0_value(uint32_t s)
+{
+    if (s == 0xffu) return __uint_as_float(0x7fc00000u);
+    return __uint_as_float(s == 0u ? 0x00400000u : (s << 23));
+}
+
+// Two E4M3 codes (element 2k in the low byte) to two binary32 values, exact.
+__device__ __forceinline__ float2 e4m3x2_to_f32x2(uint16_t codes)
+{
+    uint32_t h2;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(codes));
+    return __half22float2(*reinterpret_cast<__half2 *>(&h2));
+}
+
+// Two binary32 values to E4M3 codes, round to nearest even, saturating at
+// +-448; `lo` goes to the low byte.
+__device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi)
+{
+    uint16_t d;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(d) : "f"(hi), "f"(lo));
+    return d;
+}
+
+// ------------------------------------------------------------------ gradient sources
+//
+// A source yields, for a vector of 8 consecutive flat indices, the
+// rank-ordered fp32 sum of the P rank values (the reduce-scatter of one
+// shard element), starting from +0.
+
+template <int P>
+struct Bf16Src {
+    static constexpr int kRanks = P;
+    const uint16_t *g[P];
+
+    __device__ __forceinline__ void sum8(int64_t vec, float (&out)[kVec]) const
+    {
+        uint4 x[P];
+#pragma unroll
+        for (int r = 0; r < P; ++r) x[r] = ld_stream(reinterpret_cast<const uint4 *>(g[r]) + vec);
+#pragma unroll
+        for (int j = 0; j < kVec; ++j) out[j] = 0.0f;
+#pragma unroll
+        for (int r = 0; r < P; ++r) {
+            const uint32_t w4[4] = {x[r].x, x[r].y, x[r].z, x[r].w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                out[2 * q] = __fadd_rn(out[2 * q], bf16_lo(w4[q]));
+                out[2 * q + 1] = __fadd_rn(out[2 * q + 1], bf16_hi(w4[q]));
+            }
+        }
+    }
+
+    __device__ __forceinline__ float sum1(int64_t i) const
+    {
+        float s = 0.0f;
+#pragma unroll
+        for (int r = 0; r < P; ++r) s = __fadd_rn(s, __uint_as_float(uint32_t(g[r][i]) << 16));
+        return s;
+    }
+};
+
+template <int P>
+struct MxSrc {
+    static constexpr int kRanks = P;
+    const uint8_t *c[P];  // E4M3 codes, one byte per element
+    const uint8_t *s[P];  // E8M0 scales, one byte per 32 elements
+
+    __device__ __forceinline__ void sum8(int64_t vec, float (&out)[kVec]) const
+    {
+        uint2 x[P];
+        uint32_t sc[P];
+#pragma unroll
+        for (int r = 0; r < P; ++r) {
+            x[r] = ld_stream(reinterpret_cast<const uint2 *>(c[r]) + vec);
+            sc[r] = s[r][vec >> 2];
+        }
+#pragma unroll
+        for (int j = 0; j < kVec; ++j) out[j] = 0.0f;
+#pragma unroll
+        for (int r = 0; r < P; ++r) {
+            const float scale = e8m0_value(sc[r]);
+            const uint32_t w2[2] = {x[r].x, x[r].y};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float2 f = e4m3x2_to_f32x2(uint16_t(w2[q >> 1] >> (16 * (q & 1))));
+                out[2 * q] = __fadd_rn(out[2 * q], __fmul_rn(f.x, scale));
+                out[2 * q + 1] = __fadd_rn(out[2 * q + 1], __fmul_rn(f.y, scale));
+            }
+        }
+    }
+
+    __device__ __forceinline__ float sum1(int64_t i) const
+    {
+        float s = 0.0f;
+#pragma unroll
+        for (int r = 0; r < P; ++r) {
+            const float2 f = e4m3x2_to_f32x2(uint16_t(c[r][i]));
+            s = __fadd_rn(s, __fmul_rn(f.x, e8m0_value(this->s[r][i >> 5])));
+        }
+        return s;
+    }
+};
+
+// ------------------------------------------------------------------ reductions
+
+// Error-free accumulation of x into the unevaluated pair hi + lo (Knuth's
+// two-sum): the norm keeps about 48 bits per thread without fp64 arithmetic,
+// which GB300 runs at a small fraction of its fp32 rate.
+__device__ __forceinline__ void two_sum_acc(float &hi, float &lo, float x)
+{
+    const float s = __fadd_rn(hi, x);
+    const float bp = __fsub_rn(s, hi);
+    const float e = __fadd_rn(__fsub_rn(hi, __fsub_rn(s, bp)), __fsub_rn(x, bp));
+    hi = s;
+    lo = __fadd_rn(lo, e);
+}
+
+// Deterministic block sum of one double per thread; the result is valid in
+// thread 0. Fixed butterfly within warps, then warp 0 over the warp sums.
+template <int THREADS>
+__device__ __forceinline__ double block_sum(double x, double *smem)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
+    __syncthreads();  // earlier readers of smem are done
+    if (lane == 0) smem[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        x = lane < THREADS / 32 ? smem[lane] : 0.0;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
+    }
+    return x;
+}
+
+// ------------------------------------------------------------------ AdamW element
+
+__device__ __forceinline__ void adamw(float g, float c, float bc1, float bc2, const StepK &k,
+                                      float &w, float &m, float &v)
+{
+    const float ga = __fmul_rn(g, c);
+    const float mi = __fadd_rn(__fmul_rn(k.b1, m), __fmul_rn(k.omb1, ga));
+    const float vi = __fadd_rn(__fmul_rn(k.b2, v), __fmul_rn(k.omb2, __fmul_rn(ga, ga)));
+    const float mh = __fdiv_rn(mi, bc1);
+    const float vh = __fdiv_rn(vi, bc2);
+    const float den = __fadd_rn(__fsqrt_rn(vh), k.eps);
+    float wi = __fsub_rn(w, __fmul_rn(k.lrwd, w));
+    wi = __fsub_rn(wi, __fmul_rn(k.lr, __fdiv_rn(mh, den)));
+    m = mi;
+    v = vi;
+    w = wi;
+}
+
+// ------------------------------------------------------------------ norm pass
+
+constexpr int kNormThreads = 256;
+constexpr int kNormFlush = 4;  // vectors (32 elements) per two-sum run before widening to fp64
+
+// Finalize: runs once, in the last block of the norm pass (thread 0).
+__device__ __forceinline__ void finalize_decision(Scalars *sc, double sumsq, const FinalizeK &fk)
+{
+    const int bad = !isfinite(sumsq);
+    sc->sumsq = sumsq;
+    sc->norm = sqrt(sumsq);
+    sc->found_inf = bad;
+    if (bad) {
+        sc->t_next = sc->t;
+        sc->b1p_next = sc->b1p;
+        sc->b2p_next = sc->b2p;
+        sc->clip = 1.0f;
+        sc->bc1 = 1.0f;
+        sc->bc2 = 1.0f;
+    } else {
+        sc->t_next = sc->t + 1;
+        sc->b1p_next = sc->b1p * fk.beta1;
+        sc->b2p_next = sc->b2p * fk.beta2;
+        sc->bc1 = float(1.0 - sc->b1p_next);
+        sc->bc2 = float(1.0 - sc->b2p_next);
+        if (fk.max_grad_norm > 0.0) {
+            const double q = fk.max_grad_norm / (sc->norm + fk.norm_eps);
+            sc->clip = float(q < 1.0 ? q : 1.0);
+        } else {
+            sc->clip = 1.0f;
+        }
+    }
+    sc->norm_gen = sc->norm_gen + 1u;
+}
+
+// Grid-stride over 8-element vectors. Each thread owns a fixed set of
+// vectors (a function of N and the grid only), squares g in fp32, adds runs
+// of 32 squares with two-sum and widens each run to fp64; blocks reduce in a
+// fixed tree and the last block to finish sums the block partials in index
+// order. Same N, P and grid: bit-identical norm, run after run.
+template <class Src>
+__global__ void __launch_bounds__(kNormThreads)
+    norm_kernel(Src src, int64_t n, float inv, double *__restrict__ partials, Scalars *sc, FinalizeK fk)
+{
+    __shared__ double red[kNormThreads / 32];
+    __shared__ int am_last;
+    const int64_t nvec = n / kVec;
+    const int64_t stride = int64_t(gridDim.x) * kNormThreads;
+    int64_t v = int64_t(blockIdx.x) * kNormThreads + threadIdx.x;
+    double acc = 0.0;
+    while (v < nvec) {
+        const int64_t run_start = v;
+        float hi = 0.0f, lo = 0.0f;
+#pragma unroll 1
+        for (int k = 0; k < kNormFlush && v < nvec; ++k, v += stride) {
+            float gh[kVec];
+            src.sum8(v, gh);
+#pragma unroll
+            for (int j = 0; j < kVec; ++j) {
+                const float g = __fmul_rn(gh[j], inv);
+                two_sum_acc(hi, lo, __fmul_rn(g, g));
+            }
+        }
+        if (isfinite(hi) && isfinite(lo)) {
+            acc += double(hi);
+            acc += double(lo);
+        } else {
+            // Rare: a run whose fp32 partial overflowed or met inf/NaN. Redo
+            // it with every square widened to fp64 on its own, so the result
+            // is non-finite exactly when some square is.
+#pragma unroll 1
+            for (int64_t u = run_start; u < v; u += stride) {
+                float gh[kVec];
+                src.sum8(u, gh);
+#pragma unroll
+                for (int j = 0; j < kVec; ++j) {
+                    const float g = __fmul_rn(gh[j], inv);
+                    acc += double(__fmul_rn(g, g));
+                }
+            }
+        }
+    }
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        for (int64_t i = nvec * kVec; i < n; ++i) {  // ragged tail, fewer than 8 elements
+            const float g = __fmul_rn(src.sum1(i), inv);
+            acc += double(__fmul_rn(g, g));
+        }
+    }
+    const double bsum = block_sum<kNormThreads>(acc, red);
+    if (threadIdx.x == 0) {
+        partials[blockIdx.x] = bsum;
+        __threadfence();
+        const unsigned int ticket = atomicAdd(&sc->norm_ticket, 1u);
+        am_last = (ticket == gridDim.x - 1);
+    }
+    __syncthreads();
+    if (!am_last) return;
+    __threadfence();
+    double s = 0.0;
+    for (int i = threadIdx.x; i < int(gridDim.x); i += kNormThreads) s += __ldcg(partials + i);
+    const double total = block_sum<kNormThreads>(s, red);
+    if (threadIdx.x == 0) {
+        finalize_decision(sc, total, fk);
+        sc->norm_ticket = 0u;
+    }
+}
+
+// ------------------------------------------------------------------ fused step pass
+
+constexpr int kStepThreads = 256;
+
+// The last block of a step pass commits the step count (unless skipped) and
+// marks the norm consumed, so a repeated step pass cannot apply twice.
+__device__ __forceinline__ void step_epilogue(Scalars *sc, int skip)
+{
+    __syncthreads();
+    if (threadIdx.x != 0) return;
+    __threadfence();
+    const unsigned int ticket = atomicAdd(&sc->step_ticket, 1u);
+    if (ticket != gridDim.x - 1) return;
+    if (skip == 2) {
+        sc->status = kStatusStaleNorm;
+    } else {
+        if (skip == 0) {
+            sc->t = sc->t_next;
+            sc->b1p = sc->b1p_next;
+            sc->b2p = sc->b2p_next;
+        }
+        sc->step_gen = sc->norm_gen;
+    }
+    sc->step_ticket = 0u;
+}
+
+// Read the decision once per block: skip = 0 run, 1 found inf, 2 stale norm.
+__device__ __forceinline__ int step_prologue(const Scalars *sc, float &c, float &bc1, float &bc2)
+{
+    __shared__ int s_skip;
+    __shared__ float s_c, s_bc1, s_bc2;
+    if (threadIdx.x == 0) {
+        const int stale = sc->step_gen == sc->norm_gen;
+        s_skip = stale ? 2 : (sc->found_inf ? 1 : 0);
+        s_c = sc->clip;
+        s_bc1 = sc->bc1;
+        s_bc2 = sc->bc2;
+    }
+    __syncthreads();
+    c = s_c;
+    bc1 = s_bc1;
+    bc2 = s_bc2;
+    return s_skip;
+}
+
+template <class Src>
+__device__ __forceinline__ void step_vector(const Src &src, int64_t vec, float inv, float c, float bc1,
+                                            float bc2, const StepK &k, const State &st)
+{
+    float gh[kVec];
+    src.sum8(vec, gh);
+    float4 *w4 = reinterpret_cast<float4 *>(st.w) + 2 * vec;
+    float4 *m4 = reinterpret_cast<float4 *>(st.m) + 2 * vec;
+    float4 *v4 = reinterpret_cast<float4 *>(st.v) + 2 * vec;
+    const float4 wa = ld_stream(w4), wb = ld_stream(w4 + 1);
+    const float4 ma = ld_stream(m4), mb = ld_stream(m4 + 1);
+    const float4 va = ld_stream(v4), vb = ld_stream(v4 + 1);
+    float w[kVec] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
+    float m[kVec] = {ma.x, ma.y, ma.z, ma.w, mb.x, mb.y, mb.z, mb.w};
+    float v[kVec] = {va.x, va.y, va.z, va.w, vb.x, vb.y, vb.z, vb.w};
+#pragma unroll
+    for (int j = 0; j < kVec; ++j) adamw(__fmul_rn(gh[j], inv), c, bc1, bc2, k, w[j], m[j], v[j]);
+    st_stream(w4, make_float4(w[0], w[1], w[2], w[3]));
+    st_stream(w4 + 1, make_float4(w[4], w[5], w[6], w[7]));
+    st_stream(m4, make_float4(m[0], m[1], m[2], m[3]));
+    st_stream(m4 + 1, make_float4(m[4], m[5], m[6], m[7]));
+    st_stream(v4, make_float4(v[0], v[1], v[2], v[3]));
+    st_stream(v4 + 1, make_float4(v[4], v[5], v[6], v[7]));
+    st_stream(reinterpret_cast<uint4 *>(st.p) + vec,
+              make_uint4(pack_bf16x2(w[0], w[1]), pack_bf16x2(w[2], w[3]), pack_bf16x2(w[4], w[5]),
+                         pack_bf16x2(w[6], w[7])));
+}
+
+template <class Src>
+__device__ __forceinline__ void step_tail(const Src &src, int64_t n, float inv, float c, float bc1, float bc2,
+                                          const StepK &k, const State &st)
+{
+    for (int64_t i = (n / kVec) * kVec; i < n; ++i) {
+        float w = st.w[i], m = st.m[i], v = st.v[i];
+        adamw(__fmul_rn(src.sum1(i), inv), c, bc1, bc2, k, w, m, v);
+        st.w[i] = w;
+        st.m[i] = m;
+        st.v[i] = v;
+        st.p[i] = __bfloat16_as_ushort(__float2bfloat16_rn(w));
+    }
+}
+
+// Fused reduce-scatter + unscale + clip + AdamW + bf16 all-gather, one pass,
+// plain 128-bit loads and stores, grid-stride over 8-element vectors.
+template <class Src>
+__global__ void __launch_bounds__(kStepThreads)
+    step_kernel(Src src, int64_t n, float inv, StepK k, State st, Scalars *sc)
+{
+    float c, bc1, bc2;
+    const int skip = step_prologue(sc, c, bc1, bc2);
+    if (skip == 0) {
+        const int64_t nvec = n / kVec;
+        const int64_t stride = int64_t(gridDim.x) * kStepThreads;
+#pragma unroll 1
+        for (int64_t v = int64_t(blockIdx.x) * kStepThreads + threadIdx.x; v < nvec; v += stride)
+            step_vector(src, v, inv, c, bc1, bc2, k, st);
+        if (blockIdx.x == 0 && threadIdx.x == 0) step_tail(src, n, inv, c, bc1, bc2, k, st);
+    }
+    step_epilogue(sc, skip);
+}
+
+// ------------------------------------------------------------------ rank dispatch
+
+template <class F>
+cudaError_t with_ranks(int p, F &&f)
+{
+    switch (p) {
+#define ZG_CASE(P) \
+    case P: return f(std::integral_constant<int, P>{});
+        ZG_CASE(1) ZG_CASE(2) ZG_CASE(3) ZG_CASE(4) ZG_CASE(5) ZG_CASE(6) ZG_CASE(7) ZG_CASE(8)
+        ZG_CASE(9) ZG_CASE(10) ZG_CASE(11) ZG_CASE(12) ZG_CASE(13) ZG_CASE(14) ZG_CASE(15) ZG_CASE(16)
+#undef ZG_CASE
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace zg

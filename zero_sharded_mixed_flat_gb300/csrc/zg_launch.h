@@ -1,0 +1,29 @@
+// zg_launch.h -- host-side launchers shared by the C-ABI (internal).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "zg_kernels.cuh"
+
+namespace zg {
+
+// Grid for a grid-stride kernel: enough blocks for the work, at most one
+// full wave of resident blocks (SM count x blocks per SM).
+int wave_blocks(const void *kernel, int threads, size_t smem);
+
+cudaError_t launch_norm_bf16(int p, const uint16_t *const *g, int64_t n, float inv, double *partials,
+                             int max_blocks, Scalars *sc, FinalizeK fk, cudaStream_t st);
+cudaError_t launch_norm_mx(int p, const uint8_t *const *c, const uint8_t *const *s, int64_t n, float inv,
+                           double *partials, int max_blocks, Scalars *sc, FinalizeK fk, cudaStream_t st);
+cudaError_t launch_step_bf16(int p, const uint16_t *const *g, int64_t n, float inv, StepK k, State state,
+                             Scalars *sc, cudaStream_t st);
+cudaError_t launch_step_mx(int p, const uint8_t *const *c, const uint8_t *const *s, int64_t n, float inv,
+                           StepK k, State state, Scalars *sc, cudaStream_t st);
+cudaError_t launch_quant(const uint16_t *in, int64_t n, uint8_t *codes, uint8_t *scales, cudaStream_t st);
+cudaError_t launch_copy(const void *src, void *dst, int64_t bytes, cudaStream_t st);
+
+// Largest grid any norm launch may use (sizes the partials array).
+int norm_blocks_cap();
+
+}  // namespace zg
