@@ -220,6 +220,10 @@ int zg_shard_step(zg_ctx *ctx, const uint16_t *const *grad_ptrs, float loss_scal
     if (int rc = check_ctx(ctx, true)) return rc;
     if (int rc = check_scale(loss_scale)) return rc;
     if (int rc = check_rank_ptrs(ctx, grad_ptrs, "grad_ptrs", true)) return rc;
+    if (ctx->variant == ZG_VARIANT_TMA)
+        return finish_launch(zg::launch_step_tma(ctx->p, grad_ptrs, ctx->n, inv_scale(ctx, loss_scale), ctx->k,
+                                                 state_of(ctx), ctx->d_sc, ctx->wait_limit, stream),
+                             "TMA step pass launch");
     return finish_launch(zg::launch_step_bf16(ctx->p, grad_ptrs, ctx->n, inv_scale(ctx, loss_scale), ctx->k,
                                               state_of(ctx), ctx->d_sc, stream),
                          "step pass launch");
@@ -317,7 +321,8 @@ int zg_set_step(zg_ctx *ctx, int64_t t)
 int zg_set_variant(zg_ctx *ctx, int variant)
 {
     if (int rc = check_ctx(ctx, false)) return rc;
-    if (variant != ZG_VARIANT_LDG) return fail(ZG_ERR_INVALID_ARG, "unknown or unavailable variant %d", variant);
+    if (variant != ZG_VARIANT_LDG && variant != ZG_VARIANT_TMA)
+        return fail(ZG_ERR_INVALID_ARG, "unknown variant %d", variant);
     ctx->variant = variant;
     return ZG_OK;
 }

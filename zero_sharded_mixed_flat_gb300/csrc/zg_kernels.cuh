@@ -49,8 +49,9 @@ struct Scalars {
     unsigned int norm_gen;     // bumped by every norm finalize
     unsigned int step_gen;     // = norm_gen once a step pass consumed that norm
     int status;                // sticky device status (ZG_OK or ZG_ERR_*)
-    int pad_;
+    unsigned int step_faults;  // CTAs of the current step launch whose wait ran out
 };
+static_assert(sizeof(Scalars) == 104, "the host copies this block back; keep its size in step");
 
 struct FinalizeK {
     double beta1, beta2, max_grad_norm, norm_eps;
@@ -473,4 +474,236 @@ cudaError_t with_ranks(int p, F &&f)
     return cudaErrorInvalidValue;
 }
 
+}  // namespace zg
+
+// ------------------------------------------------------------------ TMA-staged step pass
+//
+// The same fused step, with the operands of each 2048-element tile staged
+// in shared memory by 1-D bulk asynchronous copies (cp.async.bulk, global to
+// this CTA's shared memory, completion counted in bytes on an mbarrier): P
+// bf16 gradient slices and the fp32 w, m, v. One CTA per SM walks its tiles
+// through a ring of `stages` buffers; thread 0 refills a buffer as soon as
+// every thread has finished reading it. Results go straight from registers
+// to HBM with 128-bit streaming stores.
+//
+// Every wait is bounded (`wait_limit` polls). A wait that runs out records
+// the timeout, waits (bounded again) for the copies this CTA already issued,
+// skips the rest of its work and returns; the step is then not committed.
+
+namespace zg {
+namespace tma {
+
+constexpr int kTile = 2048;          // elements per tile: 8 per thread at 256 threads
+constexpr int kThreads = 256;
+constexpr long long kDrainLimit = 1LL << 22;
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+// Make the barrier initialisation visible to the bulk-copy (async) proxy.
+__device__ __forceinline__ void fence_barrier_init()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
+{
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(done)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+// Bounded wait: true when the phase completed within `limit` polls. A
+// limit of 0 gives up without polling.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, long long limit)
+{
+    for (long long i = 0; i < limit; ++i)
+        if (mbar_try_wait(bar, parity)) return true;
+    return false;
+}
+
+struct Layout {
+    int p;
+    uint32_t grad_bytes;   // per rank per full tile
+    uint32_t stage_bytes;  // P gradient slices + w, m, v
+    __host__ __device__ static Layout of(int p)
+    {
+        Layout l;
+        l.p = p;
+        l.grad_bytes = kTile * 2;
+        l.stage_bytes = p * l.grad_bytes + 3 * kTile * 4;
+        return l;
+    }
+};
+
+template <int P>
+__global__ void __launch_bounds__(kThreads)
+    step_kernel_tma(Bf16Src<P> src, int64_t n, float inv, StepK k, State st, Scalars *sc, int stages,
+                    long long wait_limit)
+{
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ __align__(8) uint64_t bars[8];
+    __shared__ int s_timeout;
+
+    float c, bc1, bc2;
+    int skip = step_prologue(sc, c, bc1, bc2);
+    const Layout lay = Layout::of(P);
+    const int64_t nvec = n / kVec;
+    const int64_t covered = nvec * kVec;  // elements the tiles cover; the rest is the scalar tail
+    const int64_t ntiles = (covered + kTile - 1) / kTile;
+    const int64_t my_tiles = int64_t(blockIdx.x) < ntiles ? (ntiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+
+    if (threadIdx.x == 0) {
+        s_timeout = 0;
+        for (int s = 0; s < stages; ++s) mbar_init(&bars[s], 1);
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    auto stage_ptr = [&](int s) { return smem + size_t(s) * lay.stage_bytes; };
+    auto issue = [&](int64_t j) {  // thread 0: start the copies of this CTA's j-th tile
+        const int s = int(j % stages);
+        const int64_t t0 = (int64_t(blockIdx.x) + j * gridDim.x) * kTile;
+        const int64_t len = covered - t0 < kTile ? covered - t0 : kTile;
+        unsigned char *buf = stage_ptr(s);
+        const uint32_t gb = uint32_t(len * 2), fb = uint32_t(len * 4);
+        mbar_expect_tx(&bars[s], P * gb + 3 * fb);
+#pragma unroll
+        for (int r = 0; r < P; ++r) bulk_g2s(buf + r * lay.grad_bytes, src.g[r] + t0, gb, &bars[s]);
+        float *f = reinterpret_cast<float *>(buf + P * lay.grad_bytes);
+        bulk_g2s(f, st.w + t0, fb, &bars[s]);
+        bulk_g2s(f + kTile, st.m + t0, fb, &bars[s]);
+        bulk_g2s(f + 2 * kTile, st.v + t0, fb, &bars[s]);
+    };
+
+    int64_t issued = 0;
+    if (skip == 0 && threadIdx.x == 0)
+        for (; issued < my_tiles && issued < stages; ++issued) issue(issued);
+
+    bool timed_out = false;
+    int64_t consumed = 0;
+    for (int64_t j = 0; skip == 0 && j < my_tiles; ++j, consumed = j) {
+        const int s = int(j % stages);
+        const uint32_t parity = uint32_t((j / stages) & 1);
+        if (!mbar_wait(&bars[s], parity, wait_limit)) timed_out = true;
+        if (timed_out) atomicExch(&s_timeout, 1);
+        __syncthreads();
+        if (s_timeout) break;
+        const int64_t t0 = (int64_t(blockIdx.x) + j * gridDim.x) * kTile;
+        const int64_t len = covered - t0 < kTile ? covered - t0 : kTile;
+        const int e = threadIdx.x * kVec;
+        if (e < len) {
+            const unsigned char *buf = stage_ptr(s);
+            float gh[kVec];
+#pragma unroll
+            for (int q = 0; q < kVec; ++q) gh[q] = 0.0f;
+#pragma unroll
+            for (int r = 0; r < P; ++r) {
+                const uint4 x = *reinterpret_cast<const uint4 *>(buf + r * lay.grad_bytes + e * 2);
+                const uint32_t w4[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    gh[2 * q] = __fadd_rn(gh[2 * q], bf16_lo(w4[q]));
+                    gh[2 * q + 1] = __fadd_rn(gh[2 * q + 1], bf16_hi(w4[q]));
+                }
+            }
+            const float *f = reinterpret_cast<const float *>(buf + P * lay.grad_bytes);
+            float w[kVec], m[kVec], v[kVec];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const float4 a = *reinterpret_cast<const float4 *>(f + e + 4 * h);
+                const float4 b = *reinterpret_cast<const float4 *>(f + kTile + e + 4 * h);
+                const float4 d = *reinterpret_cast<const float4 *>(f + 2 * kTile + e + 4 * h);
+                w[4 * h] = a.x, w[4 * h + 1] = a.y, w[4 * h + 2] = a.z, w[4 * h + 3] = a.w;
+                m[4 * h] = b.x, m[4 * h + 1] = b.y, m[4 * h + 2] = b.z, m[4 * h + 3] = b.w;
+                v[4 * h] = d.x, v[4 * h + 1] = d.y, v[4 * h + 2] = d.z, v[4 * h + 3] = d.w;
+            }
+#pragma unroll
+            for (int q = 0; q < kVec; ++q) adamw(__fmul_rn(gh[q], inv), c, bc1, bc2, k, w[q], m[q], v[q]);
+            const int64_t gi = t0 + e;
+            float4 *w4 = reinterpret_cast<float4 *>(st.w + gi);
+            float4 *m4 = reinterpret_cast<float4 *>(st.m + gi);
+            float4 *v4 = reinterpret_cast<float4 *>(st.v + gi);
+            st_stream(w4, make_float4(w[0], w[1], w[2], w[3]));
+            st_stream(w4 + 1, make_float4(w[4], w[5], w[6], w[7]));
+            st_stream(m4, make_float4(m[0], m[1], m[2], m[3]));
+            st_stream(m4 + 1, make_float4(m[4], m[5], m[6], m[7]));
+            st_stream(v4, make_float4(v[0], v[1], v[2], v[3]));
+            st_stream(v4 + 1, make_float4(v[4], v[5], v[6], v[7]));
+            st_stream(reinterpret_cast<uint4 *>(st.p + gi),
+                      make_uint4(pack_bf16x2(w[0], w[1]), pack_bf16x2(w[2], w[3]), pack_bf16x2(w[4], w[5]),
+                                 pack_bf16x2(w[6], w[7])));
+        }
+        __syncthreads();  // everyone is done reading buffer s
+        if (threadIdx.x == 0 && issued < my_tiles) issue(issued++);
+    }
+
+    if (s_timeout) {
+        // Drain: wait (bounded) for every copy this CTA issued and has not
+        // consumed, so no bulk copy lands after the CTA is gone.
+        if (threadIdx.x == 0) {
+            for (int64_t j = consumed; j < issued; ++j) {
+                const int s = int(j % stages);
+                mbar_wait(&bars[s], uint32_t((j / stages) & 1), kDrainLimit);
+            }
+            sc->status = kStatusTimeout;
+            atomicAdd(&sc->step_faults, 1u);
+        }
+        skip = 3;
+    } else if (skip == 0 && blockIdx.x == 0 && threadIdx.x == 0) {
+        step_tail(src, n, inv, c, bc1, bc2, k, st);
+    }
+    __syncthreads();
+    // commit (or not) exactly like the plain kernel; a timeout leaves the
+    // step uncommitted and the norm consumed
+    if (threadIdx.x == 0) {
+        __threadfence();
+        const unsigned int ticket = atomicAdd(&sc->step_ticket, 1u);
+        if (ticket == gridDim.x - 1) {
+            const unsigned int faults = atomicAdd(&sc->step_faults, 0u);
+            const int any_timeout = faults != 0u;
+            sc->step_faults = 0u;
+            if (skip == 2) {
+                sc->status = kStatusStaleNorm;
+            } else {
+                if (skip == 0 && !any_timeout) {
+                    sc->t = sc->t_next;
+                    sc->b1p = sc->b1p_next;
+                    sc->b2p = sc->b2p_next;
+                }
+                sc->step_gen = sc->norm_gen;
+            }
+            sc->step_ticket = 0u;
+        }
+    }
+}
+
+}  // namespace tma
 }  // namespace zg

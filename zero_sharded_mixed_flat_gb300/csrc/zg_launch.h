@@ -18,6 +18,8 @@ cudaError_t launch_norm_mx(int p, const uint8_t *const *c, const uint8_t *const 
                            double *partials, int max_blocks, Scalars *sc, FinalizeK fk, cudaStream_t st);
 cudaError_t launch_step_bf16(int p, const uint16_t *const *g, int64_t n, float inv, StepK k, State state,
                              Scalars *sc, cudaStream_t st);
+cudaError_t launch_step_tma(int p, const uint16_t *const *g, int64_t n, float inv, StepK k, State state,
+                            Scalars *sc, long long wait_limit, cudaStream_t st);
 cudaError_t launch_step_mx(int p, const uint8_t *const *c, const uint8_t *const *s, int64_t n, float inv,
                            StepK k, State state, Scalars *sc, cudaStream_t st);
 cudaError_t launch_quant(const uint16_t *in, int64_t n, uint8_t *codes, uint8_t *scales, cudaStream_t st);

@@ -1,0 +1,32 @@
+// Fused step pass with TMA-staged operands (P = 1..16).
+#include "zg_launch.h"
+
+namespace zg {
+
+cudaError_t launch_step_tma(int p, const uint16_t *const *g, int64_t n, float inv, StepK k, State state, Scalars *sc,
+                            long long wait_limit, cudaStream_t st)
+{
+    return with_ranks(p, [&](auto rk) {
+        constexpr int P = decltype(rk)::value;
+        Bf16Src<P> src;
+        for (int r = 0; r < P; ++r) src.g[r] = g[r];
+        const tma::Layout lay = tma::Layout::of(P);
+        // as many ring buffers as fit (2..4) in the 227 KB a CTA may hold
+        const int max_dyn = 227 * 1024 - 1024;
+        int stages = max_dyn / int(lay.stage_bytes);
+        stages = stages > 4 ? 4 : stages;
+        if (stages < 2) return cudaErrorInvalidConfiguration;
+        const size_t smem = size_t(stages) * lay.stage_bytes;
+        auto *fn = &tma::step_kernel_tma<P>;
+        cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+        if (e != cudaSuccess) return e;
+        const int64_t covered = (n / kVec) * kVec;
+        const int64_t tiles = (covered + tma::kTile - 1) / tma::kTile;
+        const int wave = wave_blocks(reinterpret_cast<const void *>(fn), tma::kThreads, smem);
+        const int blocks = int(tiles < 1 ? 1 : (tiles < wave ? tiles : wave));
+        fn<<<blocks, tma::kThreads, smem, st>>>(src, n, inv, k, state, sc, stages, wait_limit);
+        return cudaGetLastError();
+    });
+}
+
+}  // namespace zg
