@@ -46,15 +46,17 @@ def _stale(out: str, deps: list[str]) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(verbose: bool = False, extra: list[str] | None = None) -> str:
-    os.makedirs(OBJ, exist_ok=True)
+def build(verbose: bool = False, extra: list[str] | None = None, out_lib: str = LIB, obj_dir: str = OBJ) -> str:
+    """Compile every .cu under csrc/ and link ``out_lib``. ``extra`` adds nvcc
+    flags (for instance -D tuning knobs); use a separate ``obj_dir`` then."""
+    os.makedirs(obj_dir, exist_ok=True)
     headers = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".h", ".cuh"))]
     headers.append(os.path.join(INCLUDE, "zg.h"))
     flags = NVCC_FLAGS + (extra or [])
     cc = nvcc()
 
     def compile_one(src: str) -> str:
-        obj = os.path.join(OBJ, os.path.basename(src).replace(".cu", ".o"))
+        obj = os.path.join(obj_dir, os.path.basename(src).replace(".cu", ".o"))
         if _stale(obj, [src, *headers, __file__]):
             cmd = [cc, *flags, "-c", src, "-o", obj]
             if verbose:
@@ -65,11 +67,11 @@ def build(verbose: bool = False, extra: list[str] | None = None) -> str:
     srcs = sources()
     with ThreadPoolExecutor(max(1, min(len(srcs), os.cpu_count() or 1))) as ex:
         objs = list(ex.map(compile_one, srcs))
-    if _stale(LIB, objs):
-        tmp = LIB + f".tmp{os.getpid()}"
+    if _stale(out_lib, objs):
+        tmp = out_lib + f".tmp{os.getpid()}"
         subprocess.run([cc, *ARCH, "-shared", "-o", tmp, *objs], check=True)
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, out_lib)
+    return out_lib
 
 
 if __name__ == "__main__":

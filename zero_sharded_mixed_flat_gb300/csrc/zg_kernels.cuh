@@ -72,8 +72,24 @@ constexpr int kStatusStaleNorm = -6;   // ZG_ERR_STALE_NORM
 
 // ------------------------------------------------------------------ loads
 
-__device__ __forceinline__ uint4 ld_stream(const uint4 *p) { return __ldcs(p); }
-__device__ __forceinline__ uint2 ld_stream(const uint2 *p) { return __ldcs(p); }
+// Streaming loads. ZG_LOAD_HINT picks the cache policy: 0 = evict-first
+// (ld.global.cs), 1 = read-only non-coherent path (ld.global.nc), 2 = plain.
+#ifndef ZG_LOAD_HINT
+#define ZG_LOAD_HINT 0
+#endif
+template <class T>
+__device__ __forceinline__ T ld_hint(const T *p)
+{
+#if ZG_LOAD_HINT == 0
+    return __ldcs(p);
+#elif ZG_LOAD_HINT == 1
+    return __ldg(p);
+#else
+    return *p;
+#endif
+}
+__device__ __forceinline__ uint4 ld_stream(const uint4 *p) { return ld_hint(p); }
+__device__ __forceinline__ uint2 ld_stream(const uint2 *p) { return ld_hint(p); }
 __device__ __forceinline__ float4 ld_stream(const float4 *p) { return __ldcs(p); }
 __device__ __forceinline__ void st_stream(float4 *p, float4 v) { __stcs(p, v); }
 __device__ __forceinline__ void st_stream(uint4 *p, uint4 v) { __stcs(p, v); }
@@ -126,16 +142,32 @@ struct Bf16Src {
     static constexpr int kRanks = P;
     const uint16_t *g[P];
 
+    struct Raw {
+        uint4 x[P];
+    };
+
+    // Issue the P 16-byte loads of one vector.
+    __device__ __forceinline__ void load(int64_t vec, Raw &raw) const
+    {
+#pragma unroll
+        for (int r = 0; r < P; ++r) raw.x[r] = ld_stream(reinterpret_cast<const uint4 *>(g[r]) + vec);
+    }
+
     __device__ __forceinline__ void sum8(int64_t vec, float (&out)[kVec]) const
     {
-        uint4 x[P];
-#pragma unroll
-        for (int r = 0; r < P; ++r) x[r] = ld_stream(reinterpret_cast<const uint4 *>(g[r]) + vec);
+        Raw raw;
+        load(vec, raw);
+        reduce(raw, out);
+    }
+
+    // Rank-ordered fp32 sums of a loaded vector.
+    __device__ __forceinline__ void reduce(const Raw &raw, float (&out)[kVec]) const
+    {
 #pragma unroll
         for (int j = 0; j < kVec; ++j) out[j] = 0.0f;
 #pragma unroll
         for (int r = 0; r < P; ++r) {
-            const uint32_t w4[4] = {x[r].x, x[r].y, x[r].z, x[r].w};
+            const uint32_t w4[4] = {raw.x[r].x, raw.x[r].y, raw.x[r].z, raw.x[r].w};
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 out[2 * q] = __fadd_rn(out[2 * q], bf16_lo(w4[q]));
@@ -159,21 +191,35 @@ struct MxSrc {
     const uint8_t *c[P];  // E4M3 codes, one byte per element
     const uint8_t *s[P];  // E8M0 scales, one byte per 32 elements
 
-    __device__ __forceinline__ void sum8(int64_t vec, float (&out)[kVec]) const
-    {
+    struct Raw {
         uint2 x[P];
         uint32_t sc[P];
+    };
+
+    __device__ __forceinline__ void load(int64_t vec, Raw &raw) const
+    {
 #pragma unroll
         for (int r = 0; r < P; ++r) {
-            x[r] = ld_stream(reinterpret_cast<const uint2 *>(c[r]) + vec);
-            sc[r] = s[r][vec >> 2];
+            raw.x[r] = ld_stream(reinterpret_cast<const uint2 *>(c[r]) + vec);
+            raw.sc[r] = s[r][vec >> 2];
         }
+    }
+
+    __device__ __forceinline__ void sum8(int64_t vec, float (&out)[kVec]) const
+    {
+        Raw raw;
+        load(vec, raw);
+        reduce(raw, out);
+    }
+
+    __device__ __forceinline__ void reduce(const Raw &raw, float (&out)[kVec]) const
+    {
 #pragma unroll
         for (int j = 0; j < kVec; ++j) out[j] = 0.0f;
 #pragma unroll
         for (int r = 0; r < P; ++r) {
-            const float scale = e8m0_value(sc[r]);
-            const uint32_t w2[2] = {x[r].x, x[r].y};
+            const float scale = e8m0_value(raw.sc[r]);
+            const uint32_t w2[2] = {raw.x[r].x, raw.x[r].y};
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 const float2 f = e4m3x2_to_f32x2(uint16_t(w2[q >> 1] >> (16 * (q & 1))));
@@ -249,7 +295,15 @@ __device__ __forceinline__ void adamw(float g, float c, float bc1, float bc2, co
 // ------------------------------------------------------------------ norm pass
 
 constexpr int kNormThreads = 256;
+#ifndef ZG_NORM_UNROLL
+#define ZG_NORM_UNROLL 2
+#endif
+#ifndef ZG_NORM_MINB
+#define ZG_NORM_MINB 1
+#endif
+constexpr int kNormUnroll = ZG_NORM_UNROLL;  // vectors whose loads are in flight together
 constexpr int kNormFlush = 4;  // vectors (32 elements) per two-sum run before widening to fp64
+static_assert(kNormFlush % kNormUnroll == 0, "a run holds whole unrolled groups");
 
 // Finalize: runs once, in the last block of the norm pass (thread 0).
 __device__ __forceinline__ void finalize_decision(Scalars *sc, double sumsq, const FinalizeK &fk)
@@ -287,7 +341,7 @@ __device__ __forceinline__ void finalize_decision(Scalars *sc, double sumsq, con
 // fixed tree and the last block to finish sums the block partials in index
 // order. Same N, P and grid: bit-identical norm, run after run.
 template <class Src>
-__global__ void __launch_bounds__(kNormThreads)
+__global__ void __launch_bounds__(kNormThreads, ZG_NORM_MINB)
     norm_kernel(Src src, int64_t n, float inv, double *__restrict__ partials, Scalars *sc, FinalizeK fk)
 {
     __shared__ double red[kNormThreads / 32];
@@ -300,13 +354,21 @@ __global__ void __launch_bounds__(kNormThreads)
         const int64_t run_start = v;
         float hi = 0.0f, lo = 0.0f;
 #pragma unroll 1
-        for (int k = 0; k < kNormFlush && v < nvec; ++k, v += stride) {
-            float gh[kVec];
-            src.sum8(v, gh);
+        for (int k = 0; k < kNormFlush && v < nvec; k += kNormUnroll, v += kNormUnroll * stride) {
+            typename Src::Raw raw[kNormUnroll];
 #pragma unroll
-            for (int j = 0; j < kVec; ++j) {
-                const float g = __fmul_rn(gh[j], inv);
-                two_sum_acc(hi, lo, __fmul_rn(g, g));
+            for (int u = 0; u < kNormUnroll; ++u)
+                if (v + u * stride < nvec) src.load(v + u * stride, raw[u]);
+#pragma unroll
+            for (int u = 0; u < kNormUnroll; ++u) {
+                if (v + u * stride >= nvec) break;
+                float gh[kVec];
+                src.reduce(raw[u], gh);
+#pragma unroll
+                for (int j = 0; j < kVec; ++j) {
+                    const float g = __fmul_rn(gh[j], inv);
+                    two_sum_acc(hi, lo, __fmul_rn(g, g));
+                }
             }
         }
         if (isfinite(hi) && isfinite(lo)) {
@@ -317,7 +379,7 @@ __global__ void __launch_bounds__(kNormThreads)
             // it with every square widened to fp64 on its own, so the result
             // is non-finite exactly when some square is.
 #pragma unroll 1
-            for (int64_t u = run_start; u < v; u += stride) {
+            for (int64_t u = run_start; u < v && u < nvec; u += stride) {
                 float gh[kVec];
                 src.sum8(u, gh);
 #pragma unroll
@@ -356,6 +418,9 @@ __global__ void __launch_bounds__(kNormThreads)
 // ------------------------------------------------------------------ fused step pass
 
 constexpr int kStepThreads = 256;
+#ifndef ZG_STEP_MINB
+#define ZG_STEP_MINB 1
+#endif
 
 // The last block of a step pass commits the step count (unless skipped) and
 // marks the norm consumed, so a repeated step pass cannot apply twice.
@@ -443,7 +508,7 @@ __device__ __forceinline__ void step_tail(const Src &src, int64_t n, float inv, 
 // Fused reduce-scatter + unscale + clip + AdamW + bf16 all-gather, one pass,
 // plain 128-bit loads and stores, grid-stride over 8-element vectors.
 template <class Src>
-__global__ void __launch_bounds__(kStepThreads)
+__global__ void __launch_bounds__(kStepThreads, ZG_STEP_MINB)
     step_kernel(Src src, int64_t n, float inv, StepK k, State st, Scalars *sc)
 {
     float c, bc1, bc2;

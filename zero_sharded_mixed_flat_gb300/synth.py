@@ -144,10 +144,8 @@ def init_weights(w: Workload, lo: int = 0, hi: int | None = None) -> np.ndarray:
     return _chunked(lo, hi, chunk, np.float32)
 
 
-def grad_values(w: Workload, step: int, rank: int, lo: int = 0, hi: int | None = None) -> np.ndarray:
-    """Rank ``rank``'s unscaled gradient values for step ``step`` (1-based) on
-    [lo, hi), as float32, before the loss scale and bf16 storage."""
-    hi = w.n if hi is None else hi
+def _grad_chunk_maker(w: Workload, step: int, rank: int):
+    """chunk index -> that chunk's unscaled float32 gradient values."""
     if w.dist == "per_tensor":
         sizes = np.array([s for _, s in gpt2_small_tensors()], dtype=np.int64)
         starts = np.concatenate([[0], np.cumsum(sizes)])
@@ -168,7 +166,14 @@ def grad_values(w: Workload, step: int, rank: int, lo: int = 0, hi: int | None =
             return z * sig[seg].astype(np.float32)
         raise ValueError(w.dist)
 
-    return _chunked(lo, hi, chunk, np.float32)
+    return chunk
+
+
+def grad_values(w: Workload, step: int, rank: int, lo: int = 0, hi: int | None = None) -> np.ndarray:
+    """Rank ``rank``'s unscaled gradient values for step ``step`` (1-based) on
+    [lo, hi), as float32, before the loss scale and bf16 storage."""
+    hi = w.n if hi is None else hi
+    return _chunked(lo, hi, _grad_chunk_maker(w, step, rank), np.float32)
 
 
 def inf_index(w: Workload, step: int) -> int | None:
@@ -189,17 +194,24 @@ def _to_bf16_bits(x: np.ndarray) -> np.ndarray:
 def grads_bf16(w: Workload, step: int, rank: int, lo: int = 0, hi: int | None = None,
                loss_scale: float | None = None) -> np.ndarray:
     """The stored gradient: bf16(f32(x) * L) on [lo, hi) (indices at or past
-    N are padding and read as +0), plus the injected +inf, if any."""
+    N are padding and read as +0), plus the injected +inf, if any. Each
+    chunk is drawn, scaled and cast on its own worker thread."""
     hi = w.n if hi is None else hi
     ls = np.float32(w.loss_scale if loss_scale is None else loss_scale)
-    vals = np.zeros(max(hi - lo, 0), dtype=np.float32)
-    top = min(hi, w.n)
-    if top > lo:
-        vals[: top - lo] = grad_values(w, step, rank, lo, top) * ls
+    make = _grad_chunk_maker(w, step, rank)
+
+    def chunk(c: int) -> np.ndarray:
+        x = make(c)
+        x *= ls
+        if (c + 1) * CHUNK > w.n:
+            x[max(0, w.n - c * CHUNK):] = 0.0
+        return _to_bf16_bits(x)
+
+    out = _chunked(lo, hi, chunk, np.uint16)
     k = inf_index(w, step)
     if k is not None and rank == w.inf_rank and lo <= k < hi:
-        vals[k - lo] = np.float32(np.inf)
-    return _to_bf16_bits(vals)
+        out[k - lo] = 0x7F80
+    return out
 
 
 def padded_len(w: Workload) -> int:
