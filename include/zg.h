@@ -176,6 +176,34 @@ int zg_set_wait_limit(zg_ctx *ctx, int64_t polls);
  * the achievable HBM bandwidth in the same run. */
 int zg_probe_copy(const void *src, void *dst, int64_t bytes, zg_stream stream);
 
+/* The norm pass for callers that cannot allocate device memory. No passage
+ * of the pages corresponds to it: it exists for callers such as a process
+ * whose framework allocator has reserved nearly all device memory, a
+ * latency-critical loop that cannot afford the synchronisation a cudaMalloc
+ * or cudaFree may imply, or a plug-in handed device buffers with no way to
+ * release memory of its own. It computes what zg_grad_norm computes for the
+ * same gradients (same kernel, same summation) and writes
+ *   out[0] = sum of squares of the unscaled, averaged gradient,
+ *   out[1] = its square root (the global norm),
+ * to `out`, a caller-owned device buffer of two doubles (8-byte aligned).
+ * A non-finite out[0] means some gradient is infinite or NaN.
+ * grad_ptrs: host array of P device pointers to bf16 buffers of N elements
+ * (16-byte aligned); 1 <= P <= 16, 1 <= N < 2^62; loss_scale finite > 0;
+ * grad_average 0 or 1. Other values are rejected with ZG_ERR_INVALID_ARG or
+ * ZG_ERR_MISALIGNED and a message in zg_last_error.
+ * It allocates nothing: no cudaMalloc, no cudaFree, no allocating library
+ * call. Its scratch is a fixed 33,024-byte array inside the library's device
+ * image (block partials for at most 4096 blocks, which bounds the launch grid,
+ * plus a result block); every GPU that loads the library holds that array
+ * until the process exits. The first call on a device looks up the array's
+ * device address (cudaGetSymbolAddress), so make that first call before any
+ * stream capture. All calls on a device share the array and each clears its
+ * result block and counter first: calls that overlap on the GPU race and
+ * must be ordered by the caller (one stream, or events). Stream-ordered; does
+ * not wait. */
+int zg_grad_norm_noalloc(const uint16_t *const *grad_ptrs, int p, int64_t n, float loss_scale, int grad_average,
+                         double *out, zg_stream stream);
+
 /* Free the context and its workspace (after the stream work using it is done). */
 void zg_destroy(zg_ctx *ctx);
 

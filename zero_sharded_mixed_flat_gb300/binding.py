@@ -103,6 +103,7 @@ def lib() -> ctypes.CDLL:
             "zg_set_variant": (ctypes.c_int, [_P, ctypes.c_int]),
             "zg_set_wait_limit": (ctypes.c_int, [_P, _I64]),
             "zg_probe_copy": (ctypes.c_int, [_P, _P, _I64, _P]),
+            "zg_grad_norm_noalloc": (ctypes.c_int, [_P, ctypes.c_int, _I64, ctypes.c_float, ctypes.c_int, _P, _P]),
             "zg_destroy": (None, [_P]),
             "zg_strerror": (ctypes.c_char_p, [ctypes.c_int]),
             "zg_last_error": (ctypes.c_char_p, []),
@@ -249,6 +250,16 @@ def zg_probe_copy(src: torch.Tensor, dst: torch.Tensor, stream=None) -> None:
     if dst.numel() * dst.element_size() < nbytes:
         raise ValueError("dst smaller than src")
     _check(lib().zg_probe_copy(src.data_ptr(), dst.data_ptr(), nbytes, _stream(stream)), "zg_probe_copy")
+
+
+def zg_grad_norm_noalloc(grads, n: int, loss_scale: float, out: torch.Tensor, grad_average: int = 1,
+                         stream=None) -> None:
+    """The norm pass without any device allocation: writes sum of squares and
+    norm into ``out`` (a CUDA float64 tensor of at least two elements)."""
+    ptrs = _ptr_array([_dev_ptr(g, torch.bfloat16, n, f"grads[{r}]") for r, g in enumerate(grads)])
+    o = _dev_ptr(out, torch.float64, 2, "out")
+    _check(lib().zg_grad_norm_noalloc(ptrs, len(grads), n, loss_scale, grad_average, o, _stream(stream)),
+           "zg_grad_norm_noalloc")
 
 
 def zg_version() -> int:

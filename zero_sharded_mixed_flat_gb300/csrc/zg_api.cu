@@ -117,6 +117,8 @@ int wave_blocks(const void *kernel, int threads, size_t smem)
 
 int norm_blocks_cap() { return kPartialsCap; }
 
+int report_error(int code, const char *msg) { return fail(code, "%s", msg); }
+
 }  // namespace zg
 
 extern "C" {

@@ -28,4 +28,8 @@ cudaError_t launch_copy(const void *src, void *dst, int64_t bytes, cudaStream_t 
 // Largest grid any norm launch may use (sizes the partials array).
 int norm_blocks_cap();
 
+// Record `msg` as the calling thread's last error text (zg_last_error) and
+// return `code`.
+int report_error(int code, const char *msg);
+
 }  // namespace zg
