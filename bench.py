@@ -218,7 +218,11 @@ def time_oracle(workload, budget_s: float, steps: int, warmup: int = 0) -> dict:
         opt = oracle.OracleOptimizer(w0)
         t0 = time.perf_counter()
         for _ in range(k):
-            opt.step(grads, workload.loss_scale)
+            if workload.mx:  # each rank encodes its gradient, then the step sums decoded values
+                enc = [oracle.mx_encode(g) for g in grads]
+                opt.step_mx([c for c, _ in enc], [s for _, s in enc], workload.loss_scale)
+            else:
+                opt.step(grads, workload.loss_scale)
         return time.perf_counter() - t0
 
     probe = min(workload.n, 1 << 16)
@@ -243,7 +247,7 @@ def bench_ours(args, rank: int, world: int, local: int) -> dict | None:
     from zero_sharded_mixed_flat_gb300 import binding as zb
 
     torch.cuda.set_device(local)
-    wl = synth.workload(args.workload)
+    wl = synth.workload(args.workload, **({"n": args.n} if args.n else {}))
     n, p, ls = wl.n, wl.p, wl.loss_scale
     total = synth.padded_len(wl)
     stream = torch.cuda.current_stream()
@@ -253,15 +257,43 @@ def bench_ours(args, rank: int, world: int, local: int) -> dict | None:
     host_t = [torch.from_numpy(h.view(np.int16)).view(torch.bfloat16) for h in host]
     dev = [h.cuda() for h in host_t]
     opt = zb.ShardedAdamW(n, p, zb.Hparams(), torch.from_numpy(synth.init_weights(wl)))
-    zb.zg_set_variant(opt.ctx, zb.ZG_VARIANT_TMA if args.variant == "tma" else zb.ZG_VARIANT_LDG)
+    if args.variant == "staged":
+        opt.use_staged()
+    else:
+        zb.zg_set_variant(opt.ctx, zb.ZG_VARIANT_TMA if args.variant == "tma" else zb.ZG_VARIANT_LDG)
+    if wl.mx:
+        codes = [torch.empty(total, dtype=torch.uint8, device="cuda") for _ in range(p)]
+        scales = [torch.empty(total // 32, dtype=torch.uint8, device="cuda") for _ in range(p)]
+
+    def run_step(ev=None):
+        """One whole step; with events, mark [start, after norm, after step]
+        (the MX path adds the per-rank encodes before the norm)."""
+        if ev is not None:
+            ev[0].record(stream)
+        if wl.mx:
+            for r in range(p):
+                zb.zg_quant_mxfp8(dev[r], codes[r], scales[r], n, stream)
+            if ev is not None:
+                ev[3].record(stream)
+            zb.zg_grad_norm_mxfp8(opt.ctx, codes, scales, ls, stream)
+        else:
+            zb.zg_grad_norm(opt.ctx, dev, ls, stream)
+        if ev is not None:
+            ev[1].record(stream)
+        if wl.mx:
+            zb.zg_shard_step_mxfp8(opt.ctx, codes, scales, ls, stream)
+        else:
+            zb.zg_shard_step(opt.ctx, dev, ls, stream)
+        if ev is not None:
+            ev[2].record(stream)
 
     for _ in range(args.warmup):
-        opt.step(dev, ls, stream)
+        run_step()
     info = opt.info(stream)
     assert info.status == 0 and not info.found_inf
 
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
     clocks = ClockSampler(local)
     clocks.start()
     torch.cuda.synchronize()
@@ -270,11 +302,7 @@ def bench_ours(args, rank: int, world: int, local: int) -> dict | None:
     clocks.region(True)
     t0 = time.perf_counter()
     for k in range(K):
-        ev[k][0].record(stream)
-        zb.zg_grad_norm(opt.ctx, dev, ls, stream)
-        ev[k][1].record(stream)
-        zb.zg_shard_step(opt.ctx, dev, ls, stream)
-        ev[k][2].record(stream)
+        run_step(ev[k])
     torch.cuda.synchronize()
     wall = time.perf_counter() - t0
     clocks.region(False)
@@ -284,14 +312,26 @@ def bench_ours(args, rank: int, world: int, local: int) -> dict | None:
     assert info.status == 0 and info.step_t == args.warmup + K, info
 
     total_ms = ev[0][0].elapsed_time(ev[K - 1][2])
-    norm_ms = sum(ev[k][0].elapsed_time(ev[k][1]) for k in range(K)) / K
+    norm_start = 3 if wl.mx else 0
+    norm_ms = sum(ev[k][norm_start].elapsed_time(ev[k][1]) for k in range(K)) / K
     step_ms = sum(ev[k][1].elapsed_time(ev[k][2]) for k in range(K)) / K
+    quant_ms = sum(ev[k][0].elapsed_time(ev[k][3]) for k in range(K)) / K if wl.mx else 0.0
     t_max = max_over_ranks(total_ms / 1e3, world)
     value = world * n * K / t_max
 
     peak, peak_kind = measured_peaks()
-    b_step = accounting.shard_step_bytes_per_param(p) * n
-    b_norm = accounting.grad_norm_bytes_per_param(p) * n
+    if wl.mx:
+        b_step = accounting.mx_shard_step_bytes_per_param(p) * n
+        b_norm = accounting.mx_grad_norm_bytes_per_param(p) * n
+        b_quant = accounting.mx_quant_bytes_per_param() * p * n
+    elif args.variant == "staged":
+        b_step = accounting.staged_shard_step_bytes_per_param() * n
+        b_norm = accounting.staged_grad_norm_bytes_per_param(p) * n
+        b_quant = 0.0
+    else:
+        b_step = accounting.shard_step_bytes_per_param(p) * n
+        b_norm = accounting.grad_norm_bytes_per_param(p) * n
+        b_quant = 0.0
     achieved = b_step / (step_ms / 1e3) / 1e9
 
     # e2e: through the C ABI with gradients coming from pinned host memory
@@ -301,7 +341,7 @@ def bench_ours(args, rank: int, world: int, local: int) -> dict | None:
     for k in range(2):
         for r in range(p):
             dev[r].copy_(pinned[r], non_blocking=True)
-        opt.step(dev, ls, stream)
+        run_step()
         opt.info(stream)
     barrier(world)
     torch.cuda.synchronize()
@@ -311,7 +351,7 @@ def bench_ours(args, rank: int, world: int, local: int) -> dict | None:
     for k in range(e2e_steps):
         for r in range(p):
             dev[r].copy_(pinned[r], non_blocking=True)
-        opt.step(dev, ls, stream)
+        run_step()
         opt.info(stream)  # device->host read of the step result; synchronises
     e1.record(stream)
     torch.cuda.synchronize()
@@ -333,28 +373,33 @@ def bench_ours(args, rank: int, world: int, local: int) -> dict | None:
     probe_gbs = 2 * src.numel() * 10 / (c0.elapsed_time(c1) / 1e3) / 1e9
     del src, dst
 
-    traffic = recorded_traffic("zg_shard_step", args.workload)
+    step_kernel = ("zg_shard_step_mxfp8" if wl.mx else
+                   "zg_shard_step_staged" if args.variant == "staged" else "zg_shard_step")
+    traffic = recorded_traffic(step_kernel, args.workload)
     out = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": t_max * 1e3 / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32", "data": "synthetic (seeded bf16 gradients, resident in HBM)",
-        "config": {"workload": args.workload, "N": n, "P": p, "loss_scale": ls, "variant": args.variant,
+        "config": {"workload": args.workload if not args.n else f"{args.workload} with N={n}", "N": n, "P": p,
+                   "loss_scale": ls, "variant": args.variant,
                    "optimizer": "AdamW lr 1e-3 b 0.9/0.999 eps 1e-8 wd 0.01 clip 1.0",
                    "l2": f"inputs larger than L2: {(total * 2 * p + n * 14) / 1e9:.2f} GB working set vs 0.129 GB L2, no flush"},
-        "roofline": {"bound": "hbm", "kernel": "zg_shard_step", "achieved": achieved, "peak": peak,
+        "roofline": {"bound": "hbm", "kernel": step_kernel, "achieved": achieved, "peak": peak,
                      "unit": "GB/s", "frac": achieved / peak, "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_kind == "measured" else "fallback 6800 GB/s",
                      "traffic": traffic, "algorithmic_bytes_per_launch": b_step,
-                     "bytes_per_param": accounting.shard_step_bytes_per_param(p)},
-        "kernels": {"zg_grad_norm_us": norm_ms * 1e3, "zg_grad_norm_gbs": b_norm / (norm_ms / 1e3) / 1e9,
-                    "zg_shard_step_us": step_ms * 1e3, "zg_shard_step_gbs": achieved,
-                    "whole_step_gbs": (b_step + b_norm) / (total_ms / K / 1e3) / 1e9,
+                     "bytes_per_param": b_step / n},
+        "kernels": {"grad_norm_us": norm_ms * 1e3, "grad_norm_gbs": b_norm / (norm_ms / 1e3) / 1e9,
+                    "shard_step_us": step_ms * 1e3, "shard_step_gbs": achieved,
+                    "whole_step_gbs": (b_step + b_norm + b_quant) / (total_ms / K / 1e3) / 1e9,
                     "probe_copy_gbs": probe_gbs},
         "e2e": e2e,
-        "gpu_launches": 2 * K,
+        "gpu_launches": (2 + (p if wl.mx else 0)) * K,
         "clocks": clk,
         "wall_s": wall,
     }
+    if wl.mx:
+        out["kernels"].update(quant_us=quant_ms * 1e3, quant_gbs=b_quant / (quant_ms / 1e3) / 1e9)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = time_oracle(wl, budget_s=2.0, steps=5)
     return out if rank == 0 else None
@@ -387,7 +432,8 @@ def main(argv=None) -> int:
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="flat16m_p8")
-    ap.add_argument("--variant", choices=["ldg", "tma"], default="ldg")
+    ap.add_argument("--variant", choices=["ldg", "tma", "staged"], default="ldg")
+    ap.add_argument("--n", type=int, default=None, help="override the workload's parameter count (small profiling runs)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     if args.steps < 1 or args.warmup < 0:

@@ -69,9 +69,10 @@ extern "C" {
 
 #define ZG_MAX_RANKS 16
 
-/* Ways to run the fused step kernel; both compute identical results. */
-#define ZG_VARIANT_LDG 0 /* 128-bit vector loads straight from HBM */
-#define ZG_VARIANT_TMA 1 /* gradient slices staged in shared memory by bulk async copies */
+/* Ways to run a bf16 step; all compute identical results. */
+#define ZG_VARIANT_LDG 0    /* fused step with 128-bit vector loads straight from HBM (default) */
+#define ZG_VARIANT_TMA 1    /* fused step with its operands staged in shared memory by bulk async copies */
+#define ZG_VARIANT_STAGED 2 /* the norm pass also stores the reduced fp32 gradient; the step reads it */
 
 typedef struct CUstream_st *zg_stream; /* same type as cudaStream_t */
 typedef struct zg_ctx zg_ctx;          /* opaque; owned by the library */
@@ -161,7 +162,19 @@ int zg_get_info(zg_ctx *ctx, zg_stream stream, zg_step_info *info);
  * Synchronises the device; no step may be in flight on this context. */
 int zg_set_step(zg_ctx *ctx, int64_t t);
 
-/* Choose the fused step kernel (ZG_VARIANT_LDG or ZG_VARIANT_TMA). */
+/* The staged variant keeps the reduce-scatter output the way a stage-two
+ * rank holds it (Zero From Scratch, item 7: the reduce-scatter leaves each
+ * rank its summed shard): the norm pass writes the unscaled, averaged fp32
+ * gradient g_i (exactly the value the fused step would compute) into
+ * `stage`, a caller-owned device buffer of N floats, 16-byte aligned, and the
+ * step pass reads 4 bytes per parameter instead of the P bf16 replicas.
+ * A whole step then moves 2P + 34 bytes per parameter instead of 4P + 26
+ * (fewer from P = 5 on). Binding only records the pointer. */
+int zg_bind_grad_stage(zg_ctx *ctx, float *stage);
+
+/* Choose how bf16 steps run: ZG_VARIANT_LDG, ZG_VARIANT_TMA or
+ * ZG_VARIANT_STAGED (which needs zg_bind_grad_stage first, else
+ * ZG_ERR_NOT_BOUND). The MX path always runs the fused plain-load kernels. */
 int zg_set_variant(zg_ctx *ctx, int variant);
 
 /* Bound, in polls, on each device-side wait of the TMA variant (default a

@@ -1,0 +1,80 @@
+"""bench.py's host-side logic on CPU: the multi-rank timing reduction over two
+gloo processes, the reference arm's JSON line, and the roofline bookkeeping."""
+import io
+import json
+import os
+import socket
+import sys
+from contextlib import redirect_stdout
+
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+import bench
+
+
+def _free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank(rank: int, port: int, out_dir: str) -> None:
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE="2",
+                      LOCAL_RANK=str(rank))
+    dist.init_process_group("gloo", rank=rank, world_size=2)
+    try:
+        assert bench.dist_env() == (rank, 2, rank)
+        bench.barrier(2)
+        t = bench.max_over_ranks(1.5 if rank == 0 else 2.25, 2)
+        with open(os.path.join(out_dir, f"r{rank}"), "w") as f:
+            f.write(repr(t))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_max_over_ranks_with_two_gloo_ranks(tmp_path):
+    mp.start_processes(_rank, args=(_free_port(), str(tmp_path)), nprocs=2, start_method="spawn")
+    assert [float(open(tmp_path / f"r{r}").read()) for r in range(2)] == [2.25, 2.25]
+
+
+def test_reference_arm_prints_the_contract_line():
+    buf = io.StringIO()
+    with redirect_stdout(buf):
+        rc = bench.main(["--impl", "reference", "--steps", "2", "--warmup", "1", "--workload", "flat65k_p4"])
+    assert rc == 0
+    line = json.loads(buf.getvalue().strip().splitlines()[-1])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert key in line, key
+    assert line["impl"] == "reference" and line["value"] > 0 and line["unit"] == "params/s"
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] == 1
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["value"] == line["value"]
+    assert line["config"]["workload"] == "flat65k_p4"
+
+
+def test_reference_arm_other_ranks_exit_without_work(monkeypatch):
+    monkeypatch.setenv("RANK", "1")
+    monkeypatch.setenv("WORLD_SIZE", "2")
+    buf = io.StringIO()
+    with redirect_stdout(buf):
+        assert bench.main(["--impl", "reference", "--steps", "1", "--warmup", "0"]) == 0
+    assert buf.getvalue() == ""
+
+
+def test_roofline_bookkeeping(monkeypatch, tmp_path):
+    peak, kind = bench.measured_peaks()
+    assert peak > 0 and kind in ("measured", "fallback")
+    h = bench.kernel_source_hash()
+    assert len(h) == 16 and h == bench.kernel_source_hash()
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    (prof / "traffic.json").write_text(json.dumps({
+        "zg_shard_step/w": {"dram_bytes_per_launch": 123.0, "src_hash": h},
+        "zg_shard_step/old": {"dram_bytes_per_launch": 9.0, "src_hash": "0" * 16}}))
+    real_root = bench.ROOT
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    os.symlink(os.path.join(real_root, "zero_sharded_mixed_flat_gb300"), tmp_path / "zero_sharded_mixed_flat_gb300")
+    assert bench.recorded_traffic("zg_shard_step", "w") == 123.0
+    assert bench.recorded_traffic("zg_shard_step", "old") is None  # counters from other sources
+    assert bench.recorded_traffic("zg_shard_step", "missing") is None

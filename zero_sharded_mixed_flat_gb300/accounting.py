@@ -113,6 +113,16 @@ def step_bytes_per_param(p: int) -> int:
     return grad_norm_bytes_per_param(p) + shard_step_bytes_per_param(p)
 
 
+def staged_grad_norm_bytes_per_param(p: int) -> int:
+    """Norm pass that also stores the reduced fp32 gradient: P bf16 reads + 4."""
+    return GRAD_BF16 * p + 4
+
+
+def staged_shard_step_bytes_per_param() -> int:
+    """Step from the stored fp32 gradient: 4 read + state read/write + bf16 p."""
+    return 4 + 2 * OPTIMIZER_STATE + PARAM_BF16
+
+
 def mx_quant_bytes_per_param() -> float:
     """Encoding one rank's bf16 gradient: bf16 read, code + scale share written."""
     return GRAD_BF16 + MX_BYTES_PER_ELEMENT

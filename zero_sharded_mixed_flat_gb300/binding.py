@@ -30,6 +30,7 @@ ZG_ERR_STALE_NORM = -6
 ZG_ERR_NO_MEMORY = -7
 ZG_VARIANT_LDG = 0
 ZG_VARIANT_TMA = 1
+ZG_VARIANT_STAGED = 2
 ZG_MAX_RANKS = 16
 
 
@@ -91,6 +92,7 @@ def lib() -> ctypes.CDLL:
             "zg_init": (ctypes.c_int, [_I64, ctypes.c_int, ctypes.POINTER(_Hp), ctypes.POINTER(_P)]),
             "zg_shard_len": (_I64, [_P]),
             "zg_bind": (ctypes.c_int, [_P, _P, _P, _P, _P]),
+            "zg_bind_grad_stage": (ctypes.c_int, [_P, _P]),
             "zg_step": (ctypes.c_int, [_P, _P, ctypes.c_float, _P]),
             "zg_grad_norm": (ctypes.c_int, [_P, _P, ctypes.c_float, _P]),
             "zg_shard_step": (ctypes.c_int, [_P, _P, ctypes.c_float, _P]),
@@ -175,6 +177,11 @@ def zg_bind(ctx: Ctx, w: torch.Tensor, m: torch.Tensor, v: torch.Tensor, params:
             _dev_ptr(v, torch.float32, ctx.n, "v"), _dev_ptr(params, torch.bfloat16, ctx.n, "params")]
     _check(lib().zg_bind(ctx.handle, *ptrs), "zg_bind")
     ctx._state = (w, m, v, params)  # keep the memory alive while bound
+
+
+def zg_bind_grad_stage(ctx: Ctx, stage: torch.Tensor) -> None:
+    _check(lib().zg_bind_grad_stage(ctx.handle, _dev_ptr(stage, torch.float32, ctx.n, "stage")), "zg_bind_grad_stage")
+    ctx._stage = stage
 
 
 def _grads(ctx: Ctx, grads) -> ctypes.Array:
@@ -282,6 +289,12 @@ class ShardedAdamW:
         self.v = torch.zeros(n, dtype=torch.float32, device=device)
         self.params = self.w.to(torch.bfloat16)
         zg_bind(self.ctx, self.w, self.m, self.v, self.params)
+
+    def use_staged(self) -> None:
+        """Switch to the staged variant (allocates the fp32 stage with torch)."""
+        self.stage = torch.empty(self.n, dtype=torch.float32, device=self.w.device)
+        zg_bind_grad_stage(self.ctx, self.stage)
+        zg_set_variant(self.ctx, ZG_VARIANT_STAGED)
 
     @property
     def shard_len(self) -> int:

@@ -25,6 +25,7 @@ struct zg_ctx {
     float *w, *m, *v;
     uint16_t *params;
     bool bound;
+    float *stage;  // caller's fp32 buffer for the staged variant, or NULL
     int device;
     zg::Scalars *d_sc;
     double *d_partials;
@@ -207,13 +208,23 @@ int zg_bind(zg_ctx *ctx, float *w, float *m, float *v, uint16_t *params_bf16)
     return ZG_OK;
 }
 
+int zg_bind_grad_stage(zg_ctx *ctx, float *stage)
+{
+    if (int rc = check_ctx(ctx, false)) return rc;
+    if (!stage) return fail(ZG_ERR_INVALID_ARG, "stage must not be NULL");
+    if (!aligned16(stage)) return fail(ZG_ERR_MISALIGNED, "stage must be 16-byte aligned");
+    ctx->stage = stage;
+    return ZG_OK;
+}
+
 int zg_grad_norm(zg_ctx *ctx, const uint16_t *const *grad_ptrs, float loss_scale, zg_stream stream)
 {
     if (int rc = check_ctx(ctx, false)) return rc;
     if (int rc = check_scale(loss_scale)) return rc;
     if (int rc = check_rank_ptrs(ctx, grad_ptrs, "grad_ptrs", true)) return rc;
     return finish_launch(zg::launch_norm_bf16(ctx->p, grad_ptrs, ctx->n, inv_scale(ctx, loss_scale), ctx->d_partials,
-                                              ctx->partials_cap, ctx->d_sc, ctx->fk, stream),
+                                              ctx->partials_cap, ctx->d_sc, ctx->fk, stream,
+                                              ctx->variant == ZG_VARIANT_STAGED ? ctx->stage : nullptr),
                          "norm pass launch");
 }
 
@@ -222,6 +233,9 @@ int zg_shard_step(zg_ctx *ctx, const uint16_t *const *grad_ptrs, float loss_scal
     if (int rc = check_ctx(ctx, true)) return rc;
     if (int rc = check_scale(loss_scale)) return rc;
     if (int rc = check_rank_ptrs(ctx, grad_ptrs, "grad_ptrs", true)) return rc;
+    if (ctx->variant == ZG_VARIANT_STAGED)
+        return finish_launch(zg::launch_step_staged(ctx->stage, ctx->n, ctx->k, state_of(ctx), ctx->d_sc, stream),
+                             "staged step pass launch");
     if (ctx->variant == ZG_VARIANT_TMA)
         return finish_launch(zg::launch_step_tma(ctx->p, grad_ptrs, ctx->n, inv_scale(ctx, loss_scale), ctx->k,
                                                  state_of(ctx), ctx->d_sc, ctx->wait_limit, stream),
@@ -323,8 +337,10 @@ int zg_set_step(zg_ctx *ctx, int64_t t)
 int zg_set_variant(zg_ctx *ctx, int variant)
 {
     if (int rc = check_ctx(ctx, false)) return rc;
-    if (variant != ZG_VARIANT_LDG && variant != ZG_VARIANT_TMA)
+    if (variant != ZG_VARIANT_LDG && variant != ZG_VARIANT_TMA && variant != ZG_VARIANT_STAGED)
         return fail(ZG_ERR_INVALID_ARG, "unknown variant %d", variant);
+    if (variant == ZG_VARIANT_STAGED && !ctx->stage)
+        return fail(ZG_ERR_NOT_BOUND, "the staged variant needs zg_bind_grad_stage first");
     ctx->variant = variant;
     return ZG_OK;
 }

@@ -22,6 +22,7 @@
 #include <stdint.h>
 
 #include <type_traits>
+#include <utility>
 
 namespace zg {
 
@@ -94,6 +95,17 @@ __device__ __forceinline__ float4 ld_stream(const float4 *p) { return __ldcs(p);
 __device__ __forceinline__ void st_stream(float4 *p, float4 v) { __stcs(p, v); }
 __device__ __forceinline__ void st_stream(uint4 *p, uint4 v) { __stcs(p, v); }
 
+// Programmatic dependent launch. A kernel launched with programmatic stream
+// serialisation may start while the kernel before it on the stream is still
+// running; pdl_wait() blocks until that kernel has completed and its writes
+// are visible (a no-op for an ordinary launch), and pdl_trigger() lets the
+// next kernel on the stream start launching its blocks.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Pull a line into L2 ahead of its load.
+__device__ __forceinline__ void prefetch_l2(const void *p) { asm volatile("prefetch.global.L2 [%0];" ::"l"(p)); }
+
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
@@ -146,6 +158,12 @@ struct Bf16Src {
         uint4 x[P];
     };
 
+    __device__ __forceinline__ void prefetch(int64_t vec) const
+    {
+#pragma unroll
+        for (int r = 0; r < P; ++r) prefetch_l2(g[r] + vec * kVec);
+    }
+
     // Issue the P 16-byte loads of one vector.
     __device__ __forceinline__ void load(int64_t vec, Raw &raw) const
     {
@@ -196,6 +214,12 @@ struct MxSrc {
         uint32_t sc[P];
     };
 
+    __device__ __forceinline__ void prefetch(int64_t vec) const
+    {
+#pragma unroll
+        for (int r = 0; r < P; ++r) prefetch_l2(c[r] + vec * kVec);
+    }
+
     __device__ __forceinline__ void load(int64_t vec, Raw &raw) const
     {
 #pragma unroll
@@ -239,6 +263,41 @@ struct MxSrc {
         }
         return s;
     }
+};
+
+// The reduce-scatter output kept from the norm pass: the unscaled, averaged
+// fp32 shard gradient g, 4 bytes per parameter (used with inv = 1).
+struct StagedSrc {
+    static constexpr int kRanks = 1;
+    const float *g;
+
+    struct Raw {
+        float4 a, b;
+    };
+
+    __device__ __forceinline__ void prefetch(int64_t vec) const { prefetch_l2(g + vec * kVec); }
+
+    __device__ __forceinline__ void load(int64_t vec, Raw &raw) const
+    {
+        const float4 *p = reinterpret_cast<const float4 *>(g) + 2 * vec;
+        raw.a = __ldcs(p);
+        raw.b = __ldcs(p + 1);
+    }
+
+    __device__ __forceinline__ void reduce(const Raw &raw, float (&out)[kVec]) const
+    {
+        out[0] = raw.a.x, out[1] = raw.a.y, out[2] = raw.a.z, out[3] = raw.a.w;
+        out[4] = raw.b.x, out[5] = raw.b.y, out[6] = raw.b.z, out[7] = raw.b.w;
+    }
+
+    __device__ __forceinline__ void sum8(int64_t vec, float (&out)[kVec]) const
+    {
+        Raw raw;
+        load(vec, raw);
+        reduce(raw, out);
+    }
+
+    __device__ __forceinline__ float sum1(int64_t i) const { return g[i]; }
 };
 
 // ------------------------------------------------------------------ reductions
@@ -296,12 +355,21 @@ __device__ __forceinline__ void adamw(float g, float c, float bc1, float bc2, co
 
 constexpr int kNormThreads = 256;
 #ifndef ZG_NORM_UNROLL
-#define ZG_NORM_UNROLL 2
-#endif
-#ifndef ZG_NORM_MINB
-#define ZG_NORM_MINB 1
+#define ZG_NORM_UNROLL 1
 #endif
 constexpr int kNormUnroll = ZG_NORM_UNROLL;  // vectors whose loads are in flight together
+
+// Resident blocks per SM the compiler must allow (caps registers per
+// thread): four 256-thread blocks while the P loads of a vector fit in 64
+// registers without spilling (P <= 8), two above that.
+template <class Src>
+struct NormMinBlocks {
+#ifdef ZG_NORM_MINB
+    static constexpr int value = ZG_NORM_MINB;
+#else
+    static constexpr int value = Src::kRanks <= 8 ? 4 : 2;
+#endif
+};
 constexpr int kNormFlush = 4;  // vectors (32 elements) per two-sum run before widening to fp64
 static_assert(kNormFlush % kNormUnroll == 0, "a run holds whole unrolled groups");
 
@@ -340,12 +408,15 @@ __device__ __forceinline__ void finalize_decision(Scalars *sc, double sumsq, con
 // of 32 squares with two-sum and widens each run to fp64; blocks reduce in a
 // fixed tree and the last block to finish sums the block partials in index
 // order. Same N, P and grid: bit-identical norm, run after run.
-template <class Src>
-__global__ void __launch_bounds__(kNormThreads, ZG_NORM_MINB)
-    norm_kernel(Src src, int64_t n, float inv, double *__restrict__ partials, Scalars *sc, FinalizeK fk)
+template <class Src, bool kStage = false>
+__global__ void __launch_bounds__(kNormThreads, NormMinBlocks<Src>::value)
+    norm_kernel(Src src, int64_t n, float inv, double *__restrict__ partials, Scalars *sc, FinalizeK fk,
+                float *__restrict__ stage = nullptr)
 {
     __shared__ double red[kNormThreads / 32];
     __shared__ int am_last;
+    pdl_wait();     // the gradients may come from the kernel just before
+    pdl_trigger();  // the step pass may start its blocks as ours retire
     const int64_t nvec = n / kVec;
     const int64_t stride = int64_t(gridDim.x) * kNormThreads;
     int64_t v = int64_t(blockIdx.x) * kNormThreads + threadIdx.x;
@@ -366,8 +437,13 @@ __global__ void __launch_bounds__(kNormThreads, ZG_NORM_MINB)
                 src.reduce(raw[u], gh);
 #pragma unroll
                 for (int j = 0; j < kVec; ++j) {
-                    const float g = __fmul_rn(gh[j], inv);
-                    two_sum_acc(hi, lo, __fmul_rn(g, g));
+                    gh[j] = __fmul_rn(gh[j], inv);
+                    two_sum_acc(hi, lo, __fmul_rn(gh[j], gh[j]));
+                }
+                if (kStage) {  // keep the reduce-scatter output for the step pass
+                    float4 *o = reinterpret_cast<float4 *>(stage) + 2 * (v + u * stride);
+                    __stcs(o, make_float4(gh[0], gh[1], gh[2], gh[3]));
+                    __stcs(o + 1, make_float4(gh[4], gh[5], gh[6], gh[7]));
                 }
             }
         }
@@ -394,6 +470,7 @@ __global__ void __launch_bounds__(kNormThreads, ZG_NORM_MINB)
         for (int64_t i = nvec * kVec; i < n; ++i) {  // ragged tail, fewer than 8 elements
             const float g = __fmul_rn(src.sum1(i), inv);
             acc += double(__fmul_rn(g, g));
+            if (kStage) stage[i] = g;
         }
     }
     const double bsum = block_sum<kNormThreads>(acc, red);
@@ -418,9 +495,18 @@ __global__ void __launch_bounds__(kNormThreads, ZG_NORM_MINB)
 // ------------------------------------------------------------------ fused step pass
 
 constexpr int kStepThreads = 256;
+
+// Resident 256-thread blocks per SM the compiler must allow. Three (up to
+// 85 registers per thread) measured best on GB300: at two the SM holds too
+// few loads in flight, at four the 64-register cap costs instruction-level
+// parallelism (sweeps at N = 2^24 and 1.2e8, P = 4 and 8).
 #ifndef ZG_STEP_MINB
-#define ZG_STEP_MINB 1
+#define ZG_STEP_MINB 3
 #endif
+template <class Src>
+struct StepMinBlocks {
+    static constexpr int value = ZG_STEP_MINB;
+};
 
 // The last block of a step pass commits the step count (unless skipped) and
 // marks the norm consumed, so a repeated step pass cannot apply twice.
@@ -508,9 +594,23 @@ __device__ __forceinline__ void step_tail(const Src &src, int64_t n, float inv, 
 // Fused reduce-scatter + unscale + clip + AdamW + bf16 all-gather, one pass,
 // plain 128-bit loads and stores, grid-stride over 8-element vectors.
 template <class Src>
-__global__ void __launch_bounds__(kStepThreads, ZG_STEP_MINB)
+__global__ void __launch_bounds__(kStepThreads, StepMinBlocks<Src>::value)
     step_kernel(Src src, int64_t n, float inv, StepK k, State st, Scalars *sc)
 {
+    // Launched as a dependent of the norm pass: warm L2 with this thread's
+    // first vector (inputs the norm pass does not write), then wait for the
+    // norm pass's decision before reading it.
+    {
+        const int64_t v0 = int64_t(blockIdx.x) * kStepThreads + threadIdx.x;
+        if (v0 < n / kVec) {
+            src.prefetch(v0);
+            prefetch_l2(st.w + v0 * kVec);
+            prefetch_l2(st.m + v0 * kVec);
+            prefetch_l2(st.v + v0 * kVec);
+        }
+    }
+    pdl_wait();
+    pdl_trigger();
     float c, bc1, bc2;
     const int skip = step_prologue(sc, c, bc1, bc2);
     if (skip == 0) {
@@ -522,6 +622,32 @@ __global__ void __launch_bounds__(kStepThreads, ZG_STEP_MINB)
         if (blockIdx.x == 0 && threadIdx.x == 0) step_tail(src, n, inv, c, bc1, bc2, k, st);
     }
     step_epilogue(sc, skip);
+}
+
+// ------------------------------------------------------------------ launch
+
+#ifndef ZG_PDL
+#define ZG_PDL 1
+#endif
+
+// Launch with programmatic stream serialisation, so the kernel's blocks can
+// start while the previous kernel on the stream finishes (each kernel waits
+// with pdl_wait() before touching that kernel's results).
+template <class... Params, class... Args>
+cudaError_t launch_dependent(void (*kernel)(Params...), int blocks, int threads, size_t smem, cudaStream_t st,
+                             Args &&...args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(blocks);
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = ZG_PDL;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
 // ------------------------------------------------------------------ rank dispatch
@@ -637,6 +763,8 @@ __global__ void __launch_bounds__(kThreads)
     __shared__ __align__(8) uint64_t bars[8];
     __shared__ int s_timeout;
 
+    pdl_wait();
+    pdl_trigger();
     float c, bc1, bc2;
     int skip = step_prologue(sc, c, bc1, bc2);
     const Layout lay = Layout::of(P);

@@ -13,13 +13,13 @@ cudaError_t launch_norm_mx(int p, const uint8_t *const *c, const uint8_t *const 
             src.c[r] = c[r];
             src.s[r] = s[r];
         }
-        const void *fn = reinterpret_cast<const void *>(&norm_kernel<MxSrc<P>>);
+        const void *fn = reinterpret_cast<const void *>(&norm_kernel<MxSrc<P>, false>);
         const int64_t want = (n / kVec + kNormThreads - 1) / kNormThreads;
         int blocks = int(want < 1 ? 1 : (want < max_blocks ? want : max_blocks));
         const int wave = wave_blocks(fn, kNormThreads, 0);
         if (blocks > wave) blocks = wave;
-        norm_kernel<MxSrc<P>><<<blocks, kNormThreads, 0, st>>>(src, n, inv, partials, sc, fk);
-        return cudaGetLastError();
+        return launch_dependent(&norm_kernel<MxSrc<P>, false>, blocks, kNormThreads, 0, st, src, n, inv, partials,
+                                sc, fk, static_cast<float *>(nullptr));
     });
 }
 

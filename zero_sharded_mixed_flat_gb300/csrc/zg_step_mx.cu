@@ -17,8 +17,7 @@ cudaError_t launch_step_mx(int p, const uint8_t *const *c, const uint8_t *const 
         const int64_t want = (n / kVec + kStepThreads - 1) / kStepThreads;
         const int wave = wave_blocks(fn, kStepThreads, 0);
         const int blocks = int(want < 1 ? 1 : (want < wave ? want : wave));
-        step_kernel<MxSrc<P>><<<blocks, kStepThreads, 0, st>>>(src, n, inv, k, state, sc);
-        return cudaGetLastError();
+        return launch_dependent(&step_kernel<MxSrc<P>>, blocks, kStepThreads, 0, st, src, n, inv, k, state, sc);
     });
 }
 

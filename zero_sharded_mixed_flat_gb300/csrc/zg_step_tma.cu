@@ -3,6 +3,11 @@
 
 namespace zg {
 
+#ifndef ZG_TMA_CTAS_PER_SM
+#define ZG_TMA_CTAS_PER_SM 2
+#endif
+constexpr int kTmaCtasPerSm = ZG_TMA_CTAS_PER_SM;
+
 cudaError_t launch_step_tma(int p, const uint16_t *const *g, int64_t n, float inv, StepK k, State state, Scalars *sc,
                             long long wait_limit, cudaStream_t st)
 {
@@ -11,9 +16,12 @@ cudaError_t launch_step_tma(int p, const uint16_t *const *g, int64_t n, float in
         Bf16Src<P> src;
         for (int r = 0; r < P; ++r) src.g[r] = g[r];
         const tma::Layout lay = tma::Layout::of(P);
-        // as many ring buffers as fit (2..4) in the 227 KB a CTA may hold
-        const int max_dyn = 227 * 1024 - 1024;
-        int stages = max_dyn / int(lay.stage_bytes);
+        // Ring buffers per CTA: as many (2..4) as fit when kTmaCtasPerSm CTAs
+        // share an SM's 228 KB, so that more warps hide each tile's compute;
+        // if two buffers do not fit that way (large P), one CTA per SM.
+        const int sm_bytes = 227 * 1024 - 1024;
+        int stages = sm_bytes / kTmaCtasPerSm / int(lay.stage_bytes);
+        if (stages < 2) stages = sm_bytes / int(lay.stage_bytes);
         stages = stages > 4 ? 4 : stages;
         if (stages < 2) return cudaErrorInvalidConfiguration;
         const size_t smem = size_t(stages) * lay.stage_bytes;
@@ -24,8 +32,7 @@ cudaError_t launch_step_tma(int p, const uint16_t *const *g, int64_t n, float in
         const int64_t tiles = (covered + tma::kTile - 1) / tma::kTile;
         const int wave = wave_blocks(reinterpret_cast<const void *>(fn), tma::kThreads, smem);
         const int blocks = int(tiles < 1 ? 1 : (tiles < wave ? tiles : wave));
-        fn<<<blocks, tma::kThreads, smem, st>>>(src, n, inv, k, state, sc, stages, wait_limit);
-        return cudaGetLastError();
+        return launch_dependent(fn, blocks, tma::kThreads, smem, st, src, n, inv, k, state, sc, stages, wait_limit);
     });
 }
 
