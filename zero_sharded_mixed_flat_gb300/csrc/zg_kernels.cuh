@@ -508,6 +508,30 @@ struct StepMinBlocks {
     static constexpr int value = ZG_STEP_MINB;
 };
 
+// Vectors whose loads a thread issues before computing any of them. The
+// fused sources already put 2P + 24 bytes per vector in flight; the staged
+// fp32 gradient only 32 + 24, so each thread takes two vectors at a time
+// (at two resident blocks per SM to keep the registers).
+#ifndef ZG_STAGED_UNROLL
+#define ZG_STAGED_UNROLL 2
+#endif
+template <class Src>
+struct StepUnroll {
+    static constexpr int value = 1;
+};
+template <>
+struct StepUnroll<StagedSrc> {
+    static constexpr int value = ZG_STAGED_UNROLL;
+};
+template <int P>
+struct StepMinBlocks<MxSrc<P>> {  // P > 8 MX operands need more than 85 registers
+    static constexpr int value = P <= 8 ? ZG_STEP_MINB : 2;
+};
+template <>
+struct StepMinBlocks<StagedSrc> {
+    static constexpr int value = ZG_STAGED_UNROLL > 1 ? 2 : ZG_STEP_MINB;
+};
+
 // The last block of a step pass commits the step count (unless skipped) and
 // marks the norm consumed, so a repeated step pass cannot apply twice.
 __device__ __forceinline__ void step_epilogue(Scalars *sc, int skip)
@@ -549,23 +573,39 @@ __device__ __forceinline__ int step_prologue(const Scalars *sc, float &c, float 
     return s_skip;
 }
 
+// One vector's operands: the gradient source's raw loads and w, m, v.
 template <class Src>
-__device__ __forceinline__ void step_vector(const Src &src, int64_t vec, float inv, float c, float bc1,
-                                            float bc2, const StepK &k, const State &st)
+struct VecData {
+    typename Src::Raw raw;
+    float4 w[2], m[2], v[2];
+};
+
+template <class Src>
+__device__ __forceinline__ void step_load(const Src &src, int64_t vec, const State &st, VecData<Src> &d)
+{
+    src.load(vec, d.raw);
+    const float4 *w4 = reinterpret_cast<const float4 *>(st.w) + 2 * vec;
+    const float4 *m4 = reinterpret_cast<const float4 *>(st.m) + 2 * vec;
+    const float4 *v4 = reinterpret_cast<const float4 *>(st.v) + 2 * vec;
+    d.w[0] = ld_stream(w4), d.w[1] = ld_stream(w4 + 1);
+    d.m[0] = ld_stream(m4), d.m[1] = ld_stream(m4 + 1);
+    d.v[0] = ld_stream(v4), d.v[1] = ld_stream(v4 + 1);
+}
+
+template <class Src>
+__device__ __forceinline__ void step_compute_store(const Src &src, int64_t vec, const VecData<Src> &d, float inv,
+                                                   float c, float bc1, float bc2, const StepK &k, const State &st)
 {
     float gh[kVec];
-    src.sum8(vec, gh);
+    src.reduce(d.raw, gh);
+    float w[kVec] = {d.w[0].x, d.w[0].y, d.w[0].z, d.w[0].w, d.w[1].x, d.w[1].y, d.w[1].z, d.w[1].w};
+    float m[kVec] = {d.m[0].x, d.m[0].y, d.m[0].z, d.m[0].w, d.m[1].x, d.m[1].y, d.m[1].z, d.m[1].w};
+    float v[kVec] = {d.v[0].x, d.v[0].y, d.v[0].z, d.v[0].w, d.v[1].x, d.v[1].y, d.v[1].z, d.v[1].w};
+#pragma unroll
+    for (int j = 0; j < kVec; ++j) adamw(__fmul_rn(gh[j], inv), c, bc1, bc2, k, w[j], m[j], v[j]);
     float4 *w4 = reinterpret_cast<float4 *>(st.w) + 2 * vec;
     float4 *m4 = reinterpret_cast<float4 *>(st.m) + 2 * vec;
     float4 *v4 = reinterpret_cast<float4 *>(st.v) + 2 * vec;
-    const float4 wa = ld_stream(w4), wb = ld_stream(w4 + 1);
-    const float4 ma = ld_stream(m4), mb = ld_stream(m4 + 1);
-    const float4 va = ld_stream(v4), vb = ld_stream(v4 + 1);
-    float w[kVec] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
-    float m[kVec] = {ma.x, ma.y, ma.z, ma.w, mb.x, mb.y, mb.z, mb.w};
-    float v[kVec] = {va.x, va.y, va.z, va.w, vb.x, vb.y, vb.z, vb.w};
-#pragma unroll
-    for (int j = 0; j < kVec; ++j) adamw(__fmul_rn(gh[j], inv), c, bc1, bc2, k, w[j], m[j], v[j]);
     st_stream(w4, make_float4(w[0], w[1], w[2], w[3]));
     st_stream(w4 + 1, make_float4(w[4], w[5], w[6], w[7]));
     st_stream(m4, make_float4(m[0], m[1], m[2], m[3]));
@@ -616,9 +656,17 @@ __global__ void __launch_bounds__(kStepThreads, StepMinBlocks<Src>::value)
     if (skip == 0) {
         const int64_t nvec = n / kVec;
         const int64_t stride = int64_t(gridDim.x) * kStepThreads;
+        constexpr int U = StepUnroll<Src>::value;
 #pragma unroll 1
-        for (int64_t v = int64_t(blockIdx.x) * kStepThreads + threadIdx.x; v < nvec; v += stride)
-            step_vector(src, v, inv, c, bc1, bc2, k, st);
+        for (int64_t v = int64_t(blockIdx.x) * kStepThreads + threadIdx.x; v < nvec; v += U * stride) {
+            VecData<Src> d[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+                if (v + u * stride < nvec) step_load(src, v + u * stride, st, d[u]);
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+                if (v + u * stride < nvec) step_compute_store(src, v + u * stride, d[u], inv, c, bc1, bc2, k, st);
+        }
         if (blockIdx.x == 0 && threadIdx.x == 0) step_tail(src, n, inv, c, bc1, bc2, k, st);
     }
     step_epilogue(sc, skip);
