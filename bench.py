@@ -239,6 +239,43 @@ def time_oracle(workload, budget_s: float, steps: int, warmup: int = 0) -> dict:
 
 # --------------------------------------------------------------------- our arm
 
+def time_variant(name: str, wl, dev, stream, warmup: int, K: int, world: int) -> dict:
+    """The same device-resident steps with another bf16 variant of the library
+    (identical results): whole-step params/s and the step pass's bandwidth."""
+    import torch
+
+    from zero_sharded_mixed_flat_gb300 import accounting, synth
+    from zero_sharded_mixed_flat_gb300 import binding as zb
+
+    n, p, ls = wl.n, wl.p, wl.loss_scale
+    opt = zb.ShardedAdamW(n, p, zb.Hparams(), torch.from_numpy(synth.init_weights(wl)))
+    if name == "staged":
+        opt.use_staged()
+        b_step = accounting.staged_shard_step_bytes_per_param() * n
+    else:
+        zb.zg_set_variant(opt.ctx, zb.ZG_VARIANT_TMA)
+        b_step = accounting.shard_step_bytes_per_param(p) * n
+    for _ in range(warmup):
+        opt.step(dev, ls, stream)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    torch.cuda.synchronize()
+    barrier(world)
+    for k in range(K):
+        ev[k][0].record(stream)
+        zb.zg_grad_norm(opt.ctx, dev, ls, stream)
+        ev[k][1].record(stream)
+        zb.zg_shard_step(opt.ctx, dev, ls, stream)
+        ev[k][2].record(stream)
+    torch.cuda.synchronize()
+    info = opt.info(stream)
+    assert info.status == 0 and info.step_t == warmup + K
+    total = max_over_ranks(ev[0][0].elapsed_time(ev[K - 1][2]) / 1e3, world)
+    step_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / K
+    return {"value": world * n * K / total, "unit": UNIT, "ms_per_step": total * 1e3 / K,
+            "shard_step_us": step_ms * 1e3, "shard_step_gbs": b_step / (step_ms / 1e3) / 1e9,
+            "shard_step_bytes_per_param": b_step / n, "gpu_launches": 2 * K}
+
+
 def bench_ours(args, rank: int, world: int, local: int) -> dict | None:
     import numpy as np
     import torch
@@ -334,30 +371,50 @@ def bench_ours(args, rank: int, world: int, local: int) -> dict | None:
         b_quant = 0.0
     achieved = b_step / (step_ms / 1e3) / 1e9
 
-    # e2e: through the C ABI with gradients coming from pinned host memory
-    # every step and the step scalars read back every step.
-    pinned = [h.pin_memory() for h in host_t]
-    e2e_steps = max(3, min(K, 200))
-    for k in range(2):
+    # e2e: through the C ABI with the step's inputs coming from pinned host
+    # memory every step and the step scalars read back every step. The bf16
+    # path's inputs are the P bf16 gradient buffers; the MX path's inputs are
+    # the encoded wire payload, codes and scales (encoded once on the GPU
+    # here and parked in host memory, as a sending rank would transmit them).
+    if args.no_e2e:
+        pass
+    elif wl.mx:
         for r in range(p):
-            dev[r].copy_(pinned[r], non_blocking=True)
-        run_step()
-        opt.info(stream)
+            zb.zg_quant_mxfp8(dev[r], codes[r], scales[r], n, stream)
+        h_in = [c[:n].cpu().pin_memory() for c in codes] + [sc[:(n + 31) // 32].cpu().pin_memory() for sc in scales]
+        d_in = [c[:n] for c in codes] + [sc[:(n + 31) // 32] for sc in scales]
+
+        def e2e_step():
+            for d, h in zip(d_in, h_in):
+                d.copy_(h, non_blocking=True)
+            zb.zg_step_mxfp8(opt.ctx, codes, scales, ls, stream)
+            opt.info(stream)  # device->host read of the step result; synchronises
+    else:
+        h_in = [h.pin_memory() for h in host_t]
+        d_in = dev
+
+        def e2e_step():
+            for d, h in zip(d_in, h_in):
+                d.copy_(h, non_blocking=True)
+            run_step()
+            opt.info(stream)  # device->host read of the step result; synchronises
+    e2e_steps = max(3, min(K, 200))
+    for _ in range(0 if args.no_e2e else 2):
+        e2e_step()
     barrier(world)
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for k in range(e2e_steps):
-        for r in range(p):
-            dev[r].copy_(pinned[r], non_blocking=True)
-        run_step()
-        opt.info(stream)  # device->host read of the step result; synchronises
+    for _ in range(0 if args.no_e2e else e2e_steps):
+        e2e_step()
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_s = max_over_ranks(e0.elapsed_time(e1) / 1e3, world)
-    e2e = {"value": world * n * e2e_steps / e2e_s, "unit": UNIT, "steps": e2e_steps,
-           "h2d_bytes_per_step": sum(h.numel() * 2 for h in host_t), "d2h_bytes_per_step": SCALARS_D2H_BYTES}
+    e2e = None if args.no_e2e else {"value": world * n * e2e_steps / e2e_s, "unit": UNIT, "steps": e2e_steps,
+           "h2d_bytes_per_step": sum(h.numel() * h.element_size() for h in h_in),
+           "d2h_bytes_per_step": SCALARS_D2H_BYTES,
+           "inputs": "MXFP8 codes + scales (the wire payload)" if wl.mx else "P bf16 gradient buffers"}
 
     # copy probe: achievable HBM bandwidth in the same process
     src = torch.empty(1 << 30, dtype=torch.uint8, device="cuda")
@@ -375,6 +432,10 @@ def bench_ours(args, rank: int, world: int, local: int) -> dict | None:
 
     step_kernel = ("zg_shard_step_mxfp8" if wl.mx else
                    "zg_shard_step_staged" if args.variant == "staged" else "zg_shard_step")
+    alternatives = {}
+    if not wl.mx and args.variant == "ldg" and not args.no_alternatives:
+        for name in ("staged", "tma"):
+            alternatives[name] = time_variant(name, wl, dev, stream, args.warmup, K, world)
     traffic = recorded_traffic(step_kernel, args.workload)
     out = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
@@ -394,6 +455,7 @@ def bench_ours(args, rank: int, world: int, local: int) -> dict | None:
                     "whole_step_gbs": (b_step + b_norm + b_quant) / (total_ms / K / 1e3) / 1e9,
                     "probe_copy_gbs": probe_gbs},
         "e2e": e2e,
+        "alternatives": alternatives,
         "gpu_launches": (2 + (p if wl.mx else 0)) * K,
         "clocks": clk,
         "wall_s": wall,
@@ -435,6 +497,8 @@ def main(argv=None) -> int:
     ap.add_argument("--variant", choices=["ldg", "tma", "staged"], default="ldg")
     ap.add_argument("--n", type=int, default=None, help="override the workload's parameter count (small profiling runs)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-alternatives", action="store_true", help="skip timing the other bf16 variants")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end leg (very large workloads)")
     args = ap.parse_args(argv)
     if args.steps < 1 or args.warmup < 0:
         ap.error("--steps must be >= 1 and --warmup >= 0")
