@@ -45,7 +45,7 @@ sys.path.insert(0, ROOT)
 METRIC = "optimizer-step params/sec"
 UNIT = "params/s"
 FALLBACK_HBM_GBS = 6800.0
-SCALARS_D2H_BYTES = 104  # sizeof the device scalar block zg_get_info copies back
+SCALARS_D2H_BYTES = 112  # sizeof the device scalar block zg_get_info copies back
 
 
 # --------------------------------------------------------------------- clocks
@@ -237,6 +237,73 @@ def time_oracle(workload, budget_s: float, steps: int, warmup: int = 0) -> dict:
             "seconds": el}
 
 
+# --------------------------------------------------------------------- bucket overlap
+
+def time_overlap(opt, wl, dev, stream, K: int, gemm_n: int = 8192) -> dict:
+    """How much of the optimizer step hides behind a backward pass when the
+    norm is taken bucket by bucket as gradients become ready.
+
+    The backward pass is stood in for by one bf16 GEMM (gemm_n^3, cuBLAS) per
+    25M-element gradient bucket, all on one stream. Serial: every GEMM, then
+    the norm pass, then the step pass. Overlapped: bucket b's norm runs on a
+    second stream as soon as GEMM b is done; the step follows the last
+    bucket. Reported: times per step and the optimizer time left exposed
+    after the backward pass (the part that cannot be hidden)."""
+    import torch
+
+    from zero_sharded_mixed_flat_gb300 import synth
+    from zero_sharded_mixed_flat_gb300 import binding as zb
+
+    ls = wl.loss_scale
+    bks = synth.buckets(wl.n)
+    a = torch.randn(gemm_n, gemm_n, device="cuda", dtype=torch.bfloat16)
+    b = torch.randn(gemm_n, gemm_n, device="cuda", dtype=torch.bfloat16)
+    c = torch.empty(gemm_n, gemm_n, device="cuda", dtype=torch.bfloat16)
+    side = torch.cuda.Stream()
+    done = [torch.cuda.Event() for _ in bks]
+
+    def backward():
+        for i in range(len(bks)):
+            torch.matmul(a, b, out=c)
+            done[i].record(stream)
+
+    def serial():
+        backward()
+        zb.zg_grad_norm(opt.ctx, dev, ls, stream)
+        zb.zg_shard_step(opt.ctx, dev, ls, stream)
+
+    def overlapped():
+        backward()
+        for i, (lo, hi) in enumerate(bks):
+            side.wait_event(done[i])
+            flags = (zb.ZG_BUCKET_FIRST if i == 0 else 0) | (zb.ZG_BUCKET_LAST if i == len(bks) - 1 else 0)
+            zb.zg_grad_norm_bucket(opt.ctx, dev, lo, hi, ls, flags, side)
+        zb.zg_shard_step(opt.ctx, dev, ls, side)
+        stream.wait_stream(side)
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(K):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / K
+
+    t_bwd = timed(backward)
+    t_serial = timed(serial)
+    t_overlap = timed(overlapped)
+    info = opt.info(stream)
+    assert info.status == 0
+    return {"buckets": len(bks), "bucket_elements": bks[0][1] - bks[0][0],
+            "backward_stand_in": f"{len(bks)} bf16 GEMMs of {gemm_n}^3 (cuBLAS), one per bucket",
+            "backward_ms": t_bwd, "serial_ms": t_serial, "overlapped_ms": t_overlap,
+            "optimizer_exposed_serial_ms": t_serial - t_bwd, "optimizer_exposed_overlapped_ms": t_overlap - t_bwd}
+
+
 # --------------------------------------------------------------------- our arm
 
 def time_variant(name: str, wl, dev, stream, warmup: int, K: int, world: int) -> dict:
@@ -293,7 +360,7 @@ def bench_ours(args, rank: int, world: int, local: int) -> dict | None:
     host = synth.step_grads(wl, 1)
     host_t = [torch.from_numpy(h.view(np.int16)).view(torch.bfloat16) for h in host]
     dev = [h.cuda() for h in host_t]
-    opt = zb.ShardedAdamW(n, p, zb.Hparams(), torch.from_numpy(synth.init_weights(wl)))
+    opt = zb.ShardedAdamW(n, p, zb.Hparams(), torch.from_numpy(synth.init_weights(wl)), offload=args.offload)
     if args.variant == "staged":
         opt.use_staged()
     else:
@@ -430,10 +497,11 @@ def bench_ours(args, rank: int, world: int, local: int) -> dict | None:
     probe_gbs = 2 * src.numel() * 10 / (c0.elapsed_time(c1) / 1e3) / 1e9
     del src, dst
 
+    overlap = time_overlap(opt, wl, dev, stream, max(3, min(K, 50))) if args.overlap and not wl.mx else None
     step_kernel = ("zg_shard_step_mxfp8" if wl.mx else
                    "zg_shard_step_staged" if args.variant == "staged" else "zg_shard_step")
     alternatives = {}
-    if not wl.mx and args.variant == "ldg" and not args.no_alternatives:
+    if not wl.mx and args.variant == "ldg" and not args.no_alternatives and not args.offload:
         for name in ("staged", "tma"):
             alternatives[name] = time_variant(name, wl, dev, stream, args.warmup, K, world)
     traffic = recorded_traffic(step_kernel, args.workload)
@@ -443,6 +511,7 @@ def bench_ours(args, rank: int, world: int, local: int) -> dict | None:
         "dtype": "f32", "data": "synthetic (seeded bf16 gradients, resident in HBM)",
         "config": {"workload": args.workload if not args.n else f"{args.workload} with N={n}", "N": n, "P": p,
                    "loss_scale": ls, "variant": args.variant,
+                   "optimizer_state": "pinned host memory (offloaded)" if args.offload else "HBM",
                    "optimizer": "AdamW lr 1e-3 b 0.9/0.999 eps 1e-8 wd 0.01 clip 1.0",
                    "l2": f"inputs larger than L2: {(total * 2 * p + n * 14) / 1e9:.2f} GB working set vs 0.129 GB L2, no flush"},
         "roofline": {"bound": "hbm", "kernel": step_kernel, "achieved": achieved, "peak": peak,
@@ -456,12 +525,17 @@ def bench_ours(args, rank: int, world: int, local: int) -> dict | None:
                     "probe_copy_gbs": probe_gbs},
         "e2e": e2e,
         "alternatives": alternatives,
+        **({"overlap": overlap} if overlap else {}),
         "gpu_launches": (2 + (p if wl.mx else 0)) * K,
         "clocks": clk,
         "wall_s": wall,
     }
     if wl.mx:
         out["kernels"].update(quant_us=quant_ms * 1e3, quant_gbs=b_quant / (quant_ms / 1e3) / 1e9)
+    if args.offload:
+        # the fp32 state crosses the host link twice per step (read, then written back)
+        out["offload"] = {"state_bytes_over_link_per_step": 24 * n,
+                          "link_gbs_in_step_pass": 24 * n / (step_ms / 1e3) / 1e9}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = time_oracle(wl, budget_s=2.0, steps=5)
     return out if rank == 0 else None
@@ -499,6 +573,10 @@ def main(argv=None) -> int:
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-alternatives", action="store_true", help="skip timing the other bf16 variants")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end leg (very large workloads)")
+    ap.add_argument("--overlap", action="store_true",
+                    help="also time the bucketed norm overlapped with a stand-in backward pass")
+    ap.add_argument("--offload", action="store_true",
+                    help="fp32 optimizer state in pinned host memory, read and written over the host link")
     args = ap.parse_args(argv)
     if args.steps < 1 or args.warmup < 0:
         ap.error("--steps must be >= 1 and --warmup >= 0")

@@ -105,8 +105,11 @@ int zg_init(int64_t n, int p, const zg_hparams *hp, zg_ctx **out);
 int64_t zg_shard_len(const zg_ctx *ctx);
 
 /* Attach the caller's optimizer state: fp32 master weights w, moments m and
- * v, and the bf16 parameter buffer (each N elements, 16-byte aligned,
- * device memory). The library keeps the pointers, never the memory. */
+ * v, and the bf16 parameter buffer (each N elements, 16-byte aligned). The
+ * library keeps the pointers, never the memory. params must be device
+ * memory. w, m and v may be device memory or pinned, device-accessible host
+ * memory: optimizer state moved off the card (Zero From Scratch, item 11),
+ * which the step kernels then read and write in place over the host link. */
 int zg_bind(zg_ctx *ctx, float *w, float *m, float *v, uint16_t *params_bf16);
 
 /* One whole step: zg_grad_norm then zg_shard_step on `stream`.
@@ -120,6 +123,26 @@ int zg_step(zg_ctx *ctx, const uint16_t *const *grad_ptrs, float loss_scale, zg_
  * partials), the found-inf decision, the clip factor and the next bias
  * corrections, all left in device memory. Reads 2P bytes per parameter. */
 int zg_grad_norm(zg_ctx *ctx, const uint16_t *const *grad_ptrs, float loss_scale, zg_stream stream);
+
+/* The first half of a step taken bucket by bucket, so each bucket's share of
+ * the norm can be computed while later layers are still producing their
+ * gradients (Zero From Scratch, item 13: sending each bucket while later
+ * layers compute). The clip needs the norm of all N, so the AdamW update
+ * still waits for the last bucket: that bucket's norm and the step pass are
+ * the part that cannot be hidden. Buckets are contiguous flat ranges
+ * [lo, hi) submitted in order on one stream: the first carries
+ * ZG_BUCKET_FIRST and starts at 0, each next starts where the previous
+ * ended, the last carries ZG_BUCKET_LAST and ends at N (one bucket may carry
+ * both). lo must be a multiple of 8. Each bucket's sum of squares is added,
+ * in submission order, to a running fp64 sum on the device; the last bucket
+ * makes the same decision zg_grad_norm makes. grad_ptrs point at the start of
+ * the full P buffers (not at the bucket). Out-of-order, gapped or unterminated
+ * sequences are refused with ZG_ERR_INVALID_ARG before anything launches.
+ * With ZG_VARIANT_STAGED each bucket also stores its part of the gradient. */
+#define ZG_BUCKET_FIRST 1
+#define ZG_BUCKET_LAST 2
+int zg_grad_norm_bucket(zg_ctx *ctx, const uint16_t *const *grad_ptrs, int64_t lo, int64_t hi, float loss_scale,
+                        int flags, zg_stream stream);
 
 /* Second half: the fused reduce-scatter + unscale + clip + AdamW + bf16
  * all-gather over every shard, using the decision of the preceding

@@ -32,6 +32,8 @@ ZG_VARIANT_LDG = 0
 ZG_VARIANT_TMA = 1
 ZG_VARIANT_STAGED = 2
 ZG_MAX_RANKS = 16
+ZG_BUCKET_FIRST = 1
+ZG_BUCKET_LAST = 2
 
 
 class ZgError(RuntimeError):
@@ -96,6 +98,7 @@ def lib() -> ctypes.CDLL:
             "zg_step": (ctypes.c_int, [_P, _P, ctypes.c_float, _P]),
             "zg_grad_norm": (ctypes.c_int, [_P, _P, ctypes.c_float, _P]),
             "zg_shard_step": (ctypes.c_int, [_P, _P, ctypes.c_float, _P]),
+            "zg_grad_norm_bucket": (ctypes.c_int, [_P, _P, _I64, _I64, ctypes.c_float, ctypes.c_int, _P]),
             "zg_quant_mxfp8": (ctypes.c_int, [_P, _I64, _P, _P, _P]),
             "zg_step_mxfp8": (ctypes.c_int, [_P, _P, _P, ctypes.c_float, _P]),
             "zg_grad_norm_mxfp8": (ctypes.c_int, [_P, _P, _P, ctypes.c_float, _P]),
@@ -131,9 +134,11 @@ def _stream(stream) -> int:
     return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
 
 
-def _dev_ptr(t: torch.Tensor, dtype: torch.dtype, min_numel: int, what: str) -> int:
-    if not isinstance(t, torch.Tensor) or not t.is_cuda:
-        raise TypeError(f"{what} must be a CUDA tensor")
+def _dev_ptr(t: torch.Tensor, dtype: torch.dtype, min_numel: int, what: str, host_ok: bool = False) -> int:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{what} must be a tensor")
+    if not t.is_cuda and not (host_ok and t.is_pinned()):
+        raise TypeError(f"{what} must be a CUDA tensor" + (" or pinned host memory" if host_ok else ""))
     if t.dtype != dtype:
         raise TypeError(f"{what} must have dtype {dtype} (got {t.dtype})")
     if not t.is_contiguous():
@@ -173,8 +178,10 @@ def zg_shard_len(ctx: Ctx) -> int:
 
 
 def zg_bind(ctx: Ctx, w: torch.Tensor, m: torch.Tensor, v: torch.Tensor, params: torch.Tensor) -> None:
-    ptrs = [_dev_ptr(w, torch.float32, ctx.n, "w"), _dev_ptr(m, torch.float32, ctx.n, "m"),
-            _dev_ptr(v, torch.float32, ctx.n, "v"), _dev_ptr(params, torch.bfloat16, ctx.n, "params")]
+    """w, m, v may be CUDA tensors or pinned host tensors (optimizer state
+    offloaded to host memory, read and written by the kernels in place)."""
+    ptrs = [_dev_ptr(w, torch.float32, ctx.n, "w", True), _dev_ptr(m, torch.float32, ctx.n, "m", True),
+            _dev_ptr(v, torch.float32, ctx.n, "v", True), _dev_ptr(params, torch.bfloat16, ctx.n, "params")]
     _check(lib().zg_bind(ctx.handle, *ptrs), "zg_bind")
     ctx._state = (w, m, v, params)  # keep the memory alive while bound
 
@@ -205,6 +212,11 @@ def zg_step(ctx: Ctx, grads, loss_scale: float, stream=None) -> None:
 
 def zg_grad_norm(ctx: Ctx, grads, loss_scale: float, stream=None) -> None:
     _check(lib().zg_grad_norm(ctx.handle, _grads(ctx, grads), loss_scale, _stream(stream)), "zg_grad_norm")
+
+
+def zg_grad_norm_bucket(ctx: Ctx, grads, lo: int, hi: int, loss_scale: float, flags: int, stream=None) -> None:
+    _check(lib().zg_grad_norm_bucket(ctx.handle, _grads(ctx, grads), lo, hi, loss_scale, flags, _stream(stream)),
+           "zg_grad_norm_bucket")
 
 
 def zg_shard_step(ctx: Ctx, grads, loss_scale: float, stream=None) -> None:
@@ -277,17 +289,27 @@ def zg_version() -> int:
 
 class ShardedAdamW:
     """A context plus torch-allocated state: fp32 w, m, v and bf16 params,
-    each N long on the current CUDA device, bound to the context."""
+    each N long, bound to the context. With ``offload`` the fp32 state lives
+    in pinned host memory and the kernels read and write it there."""
 
     def __init__(self, n: int, p: int, hp: Hparams = Hparams(), w0: torch.Tensor | None = None,
-                 device: str | torch.device = "cuda"):
+                 device: str | torch.device = "cuda", offload: bool = False):
         self.ctx = zg_init(n, p, hp)
         self.n, self.p, self.hp = n, p, hp
-        self.w = (w0.to(device=device, dtype=torch.float32).contiguous().clone() if w0 is not None
-                  else torch.zeros(n, dtype=torch.float32, device=device))
-        self.m = torch.zeros(n, dtype=torch.float32, device=device)
-        self.v = torch.zeros(n, dtype=torch.float32, device=device)
-        self.params = self.w.to(torch.bfloat16)
+
+        def state(init=None):
+            if offload:
+                t = torch.zeros(n, dtype=torch.float32, pin_memory=True)
+            else:
+                t = torch.zeros(n, dtype=torch.float32, device=device)
+            if init is not None:
+                t.copy_(init.to(torch.float32).reshape(-1))
+            return t
+
+        self.w = state(w0)
+        self.m = state()
+        self.v = state()
+        self.params = self.w.to(device=device, dtype=torch.bfloat16)
         zg_bind(self.ctx, self.w, self.m, self.v, self.params)
 
     def use_staged(self) -> None:

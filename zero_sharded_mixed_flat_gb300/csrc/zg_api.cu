@@ -26,6 +26,8 @@ struct zg_ctx {
     uint16_t *params;
     bool bound;
     float *stage;  // caller's fp32 buffer for the staged variant, or NULL
+    int64_t bucket_next;  // where the next bucket of an open bucketed norm must start
+    bool bucket_open;     // a bucketed norm has started and not yet seen its last bucket
     int device;
     zg::Scalars *d_sc;
     double *d_partials;
@@ -226,6 +228,44 @@ int zg_grad_norm(zg_ctx *ctx, const uint16_t *const *grad_ptrs, float loss_scale
                                               ctx->partials_cap, ctx->d_sc, ctx->fk, stream,
                                               ctx->variant == ZG_VARIANT_STAGED ? ctx->stage : nullptr),
                          "norm pass launch");
+}
+
+int zg_grad_norm_bucket(zg_ctx *ctx, const uint16_t *const *grad_ptrs, int64_t lo, int64_t hi, float loss_scale,
+                        int flags, zg_stream stream)
+{
+    if (int rc = check_ctx(ctx, false)) return rc;
+    if (int rc = check_scale(loss_scale)) return rc;
+    if (int rc = check_rank_ptrs(ctx, grad_ptrs, "grad_ptrs", true)) return rc;
+    if (flags & ~(ZG_BUCKET_FIRST | ZG_BUCKET_LAST)) return fail(ZG_ERR_INVALID_ARG, "unknown bucket flags %d", flags);
+    if (lo < 0 || hi <= lo || hi > ctx->n)
+        return fail(ZG_ERR_INVALID_ARG, "bucket [%lld, %lld) must be a non-empty range inside [0, N)", (long long)lo,
+                    (long long)hi);
+    if (lo % 8) return fail(ZG_ERR_INVALID_ARG, "bucket starts must be multiples of 8 elements (got %lld)", (long long)lo);
+    if (flags & ZG_BUCKET_FIRST) {
+        if (lo != 0) return fail(ZG_ERR_INVALID_ARG, "the first bucket must start at 0");
+    } else {
+        if (!ctx->bucket_open)
+            return fail(ZG_ERR_INVALID_ARG, "no bucketed norm is open (the first bucket carries ZG_BUCKET_FIRST)");
+        if (lo != ctx->bucket_next)
+            return fail(ZG_ERR_INVALID_ARG, "buckets must be contiguous and in order: expected start %lld, got %lld",
+                        (long long)ctx->bucket_next, (long long)lo);
+    }
+    if ((flags & ZG_BUCKET_LAST) && hi != ctx->n) return fail(ZG_ERR_INVALID_ARG, "the last bucket must end at N");
+    if (!(flags & ZG_BUCKET_LAST) && hi == ctx->n)
+        return fail(ZG_ERR_INVALID_ARG, "a bucket that ends at N must carry ZG_BUCKET_LAST");
+    const uint16_t *g[ZG_MAX_RANKS];
+    for (int r = 0; r < ctx->p; ++r) g[r] = grad_ptrs[r] + lo;
+    float *stage = ctx->variant == ZG_VARIANT_STAGED ? ctx->stage + lo : nullptr;
+    const int mode = zg::kNormBucket | ((flags & ZG_BUCKET_FIRST) ? zg::kNormFirst : 0) |
+                     ((flags & ZG_BUCKET_LAST) ? zg::kNormLast : 0);
+    const int rc = finish_launch(zg::launch_norm_bf16(ctx->p, g, hi - lo, inv_scale(ctx, loss_scale), ctx->d_partials,
+                                                      ctx->partials_cap, ctx->d_sc, ctx->fk, stream, stage, mode),
+                                 "bucket norm launch");
+    if (rc == ZG_OK) {
+        ctx->bucket_open = !(flags & ZG_BUCKET_LAST);
+        ctx->bucket_next = hi;
+    }
+    return rc;
 }
 
 int zg_shard_step(zg_ctx *ctx, const uint16_t *const *grad_ptrs, float loss_scale, zg_stream stream)

@@ -51,8 +51,17 @@ struct Scalars {
     unsigned int step_gen;     // = norm_gen once a step pass consumed that norm
     int status;                // sticky device status (ZG_OK or ZG_ERR_*)
     unsigned int step_faults;  // CTAs of the current step launch whose wait ran out
+    double bucket_acc;         // running sum of squares over the buckets submitted so far
 };
-static_assert(sizeof(Scalars) == 104, "the host copies this block back; keep its size in step");
+static_assert(sizeof(Scalars) == 112, "the host copies this block back; keep its size in step");
+
+// How a norm launch ends: kNormWhole finalizes its own total; a bucket
+// launch (kNormBucket) adds its total to bucket_acc in submission order,
+// restarting the sum on kNormFirst and finalizing on kNormLast.
+constexpr int kNormWhole = 0;
+constexpr int kNormFirst = 1;
+constexpr int kNormLast = 2;
+constexpr int kNormBucket = 4;
 
 struct FinalizeK {
     double beta1, beta2, max_grad_norm, norm_eps;
@@ -411,7 +420,7 @@ __device__ __forceinline__ void finalize_decision(Scalars *sc, double sumsq, con
 template <class Src, bool kStage = false>
 __global__ void __launch_bounds__(kNormThreads, NormMinBlocks<Src>::value)
     norm_kernel(Src src, int64_t n, float inv, double *__restrict__ partials, Scalars *sc, FinalizeK fk,
-                float *__restrict__ stage = nullptr)
+                float *__restrict__ stage = nullptr, int mode = kNormWhole)
 {
     __shared__ double red[kNormThreads / 32];
     __shared__ int am_last;
@@ -487,7 +496,13 @@ __global__ void __launch_bounds__(kNormThreads, NormMinBlocks<Src>::value)
     for (int i = threadIdx.x; i < int(gridDim.x); i += kNormThreads) s += __ldcg(partials + i);
     const double total = block_sum<kNormThreads>(s, red);
     if (threadIdx.x == 0) {
-        finalize_decision(sc, total, fk);
+        if (!(mode & kNormBucket)) {
+            finalize_decision(sc, total, fk);
+        } else {
+            const double acc = (mode & kNormFirst) ? total : sc->bucket_acc + total;
+            sc->bucket_acc = acc;
+            if (mode & kNormLast) finalize_decision(sc, acc, fk);
+        }
         sc->norm_ticket = 0u;
     }
 }

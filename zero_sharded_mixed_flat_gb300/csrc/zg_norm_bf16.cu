@@ -4,7 +4,7 @@
 namespace zg {
 
 cudaError_t launch_norm_bf16(int p, const uint16_t *const *g, int64_t n, float inv, double *partials,
-                             int max_blocks, Scalars *sc, FinalizeK fk, cudaStream_t st, float *stage)
+                             int max_blocks, Scalars *sc, FinalizeK fk, cudaStream_t st, float *stage, int mode)
 {
     return with_ranks(p, [&](auto rk) {
         constexpr int P = decltype(rk)::value;
@@ -15,7 +15,7 @@ cudaError_t launch_norm_bf16(int p, const uint16_t *const *g, int64_t n, float i
         int blocks = int(want < 1 ? 1 : (want < max_blocks ? want : max_blocks));
         const int wave = wave_blocks(reinterpret_cast<const void *>(kernel), kNormThreads, 0);
         if (blocks > wave) blocks = wave;
-        return launch_dependent(kernel, blocks, kNormThreads, 0, st, src, n, inv, partials, sc, fk, stage);
+        return launch_dependent(kernel, blocks, kNormThreads, 0, st, src, n, inv, partials, sc, fk, stage, mode);
     });
 }
 

@@ -19,7 +19,7 @@ cudaError_t launch_norm_mx(int p, const uint8_t *const *c, const uint8_t *const 
         const int wave = wave_blocks(fn, kNormThreads, 0);
         if (blocks > wave) blocks = wave;
         return launch_dependent(&norm_kernel<MxSrc<P>, false>, blocks, kNormThreads, 0, st, src, n, inv, partials,
-                                sc, fk, static_cast<float *>(nullptr));
+                                sc, fk, static_cast<float *>(nullptr), kNormWhole);
     });
 }
 
