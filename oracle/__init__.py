@@ -86,6 +86,7 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
         "orc_e4m3_value": (ctypes.c_double, [ctypes.c_uint8]),
         "orc_e4m3_encode": (ctypes.c_uint8, [ctypes.c_double]),
         "orc_mx_encode": (None, [_P, _I64, _P, _P]),
+        "orc_mx_encode_f32": (None, [_P, _I64, _P, _P]),
         "orc_mx_decode": (ctypes.c_float, [ctypes.c_uint8, ctypes.c_uint8]),
         "orc_inv_scale": (ctypes.c_float, [ctypes.c_float, ctypes.c_int, ctypes.c_int]),
         "orc_reduce_unscale": (None, [ctypes.c_int, _P, _I64, _I64, ctypes.c_float, _P]),
@@ -198,6 +199,18 @@ def mx_encode(x_bf16: np.ndarray, lib=None):
     codes = np.zeros(n, dtype=np.uint8)
     scales = np.zeros((n + 31) // 32, dtype=np.uint8)
     lib.orc_mx_encode(_ptr(x), n, _ptr(codes), _ptr(scales))
+    return codes, scales
+
+
+def mx_encode_f32(x: np.ndarray, lib=None):
+    """MXFP8-encode float32 values (the master weights stored as MX
+    parameters; Zero From Scratch, item 14). Returns (codes, scales)."""
+    lib = lib or load()
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    n = x.size
+    codes = np.zeros(n, dtype=np.uint8)
+    scales = np.zeros((n + 31) // 32, dtype=np.uint8)
+    lib.orc_mx_encode_f32(_ptr(x), n, _ptr(codes), _ptr(scales))
     return codes, scales
 
 

@@ -170,53 +170,74 @@ uint8_t orc_e4m3_encode(double y)
 /* MXFP8 wire format (Zero From Scratch, item 14).                     */
 /* ------------------------------------------------------------------ */
 
-/* Encode x[0..n) block by block. Block k covers [32k, 32k+32); elements at or
- * past n count as zero for the block's amax and get no code written.
+/* Encode one block of cnt <= 32 values (as doubles, exact). Elements past
+ * cnt count as zero for the amax and get no code.
  * Scale rule (reading, the OCP MX v1.0 rule): e = floor(log2 amax) - 8, where
  * 8 is the exponent of E4M3's largest binade, clamped to [-127, 127]; the
  * scale byte is the E8M0 pattern e + 127 and code j is E4M3(x_j * 2^-e) with
  * saturation. An all-zero block takes e = -127. A block holding any infinity
  * or NaN takes scale byte 0xFF (E8M0 NaN) and NaN codes 0x7F, so it decodes
  * to NaN and trips the step's found-inf check. */
-void orc_mx_encode(const uint16_t *x, int64_t n, uint8_t *codes, uint8_t *scales)
+static void mx_encode_block(const double *vals, int cnt, uint8_t *codes, uint8_t *scale)
 {
     const int emax_elem = 8; /* 448 = 1.75 * 2^8 */
-    int64_t nblocks = (n + 31) / 32;
-    for (int64_t b = 0; b < nblocks; ++b) {
-        int64_t lo = 32 * b;
-        int64_t hi = lo + 32 < n ? lo + 32 : n;
-        double amax = 0.0;
-        int nonfinite = 0;
-        for (int64_t i = lo; i < hi; ++i) {
-            double xi = (double)orc_bf16_to_f32(x[i]);
-            if (!isfinite(xi))
-                nonfinite = 1;
-            else if (fabs(xi) > amax)
-                amax = fabs(xi);
-        }
-        if (nonfinite) {
-            scales[b] = 0xff;
-            for (int64_t i = lo; i < hi; ++i)
-                codes[i] = 0x7f;
-            continue;
-        }
-        int e;
-        if (amax == 0.0) {
+    double amax = 0.0;
+    int nonfinite = 0;
+    for (int j = 0; j < cnt; ++j) {
+        if (!isfinite(vals[j]))
+            nonfinite = 1;
+        else if (fabs(vals[j]) > amax)
+            amax = fabs(vals[j]);
+    }
+    if (nonfinite) {
+        *scale = 0xff;
+        for (int j = 0; j < cnt; ++j)
+            codes[j] = 0x7f;
+        return;
+    }
+    int e;
+    if (amax == 0.0) {
+        e = -127;
+    } else {
+        int k;
+        (void)frexp(amax, &k);
+        e = (k - 1) - emax_elem;
+        if (e < -127)
             e = -127;
-        } else {
-            int k;
-            (void)frexp(amax, &k);
-            e = (k - 1) - emax_elem;
-            if (e < -127)
-                e = -127;
-            if (e > 127)
-                e = 127;
-        }
-        scales[b] = (uint8_t)(e + 127);
-        for (int64_t i = lo; i < hi; ++i) {
-            double y = ldexp((double)orc_bf16_to_f32(x[i]), -e); /* exact */
-            codes[i] = orc_e4m3_encode(y);
-        }
+        if (e > 127)
+            e = 127;
+    }
+    *scale = (uint8_t)(e + 127);
+    for (int j = 0; j < cnt; ++j)
+        codes[j] = orc_e4m3_encode(ldexp(vals[j], -e)); /* the scaling is exact */
+}
+
+/* Encode one rank's bf16 buffer x[0..n) block by block (the wire format of
+ * the gradients). Block k covers [32k, 32k+32); the last block may be short. */
+void orc_mx_encode(const uint16_t *x, int64_t n, uint8_t *codes, uint8_t *scales)
+{
+    double vals[32];
+    for (int64_t b = 0; b < (n + 31) / 32; ++b) {
+        int64_t lo = 32 * b;
+        int cnt = (int)(lo + 32 < n ? 32 : n - lo);
+        for (int j = 0; j < cnt; ++j)
+            vals[j] = (double)orc_bf16_to_f32(x[lo + j]);
+        mx_encode_block(vals, cnt, codes + lo, scales + b);
+    }
+}
+
+/* The same format for fp32 values: the master weights stored as MXFP8
+ * parameters in place of bf16 (Zero From Scratch, item 14: MXFP8 on stored
+ * state). Every binary32 value is exact as a double. */
+void orc_mx_encode_f32(const float *x, int64_t n, uint8_t *codes, uint8_t *scales)
+{
+    double vals[32];
+    for (int64_t b = 0; b < (n + 31) / 32; ++b) {
+        int64_t lo = 32 * b;
+        int cnt = (int)(lo + 32 < n ? 32 : n - lo);
+        for (int j = 0; j < cnt; ++j)
+            vals[j] = (double)x[lo + j];
+        mx_encode_block(vals, cnt, codes + lo, scales + b);
     }
 }
 

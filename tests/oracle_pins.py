@@ -353,6 +353,45 @@ def pin_mx_loss_scale_shifts_scale_only(lib):
     assert np.array_equal(s2.astype(int) - s1.astype(int), np.full(s1.size, 10))
 
 
+def pin_mx_f32_encoder(lib):
+    """The MX block rule on fp32 values (stored MX parameters)."""
+    f32 = lambda v: np.array(v, dtype=np.float32)
+    # amax 1.0 -> e = -8, y = 256 x. 1 + 2^-4 -> y = 272, a tie between 256 and
+    # 288 -> even -> 256 (0x78); one fp32 ulp more breaks the tie upwards.
+    x = np.zeros(32, np.float32)
+    x[:3] = [1.0, 1.0 + 2.0 ** -4, np.nextafter(F32(1.0 + 2.0 ** -4), F32(2.0))]
+    codes, sc = oracle.mx_encode_f32(x, lib=lib)
+    assert sc[0] == 119 and list(codes[:3]) == [0x78, 0x78, 0x79]
+    # largest finite fp32 binade: e = 127 - 8 = 119, byte 246
+    codes, sc = oracle.mx_encode_f32(f32([3.0e38, -1.0e38]), lib=lib)
+    assert sc[0] == 246 and codes[0] == 0x7E and codes[1] & 0x80
+    # an fp32-subnormal block clamps at 2^-127: 2^-140 * 2^127 = 2^-13 -> 0;
+    # -2^-135 * 2^127 = -2^-8 = -(2 * 2^-9), the subnormal code 0x82; the
+    # smallest fp32 subnormal -2^-149 -> -2^-22 -> -0
+    codes, sc = oracle.mx_encode_f32(f32([2.0 ** -140, -(2.0 ** -135), -(2.0 ** -149)]), lib=lib)
+    assert sc[0] == 0 and list(codes[:3]) == [0x00, 0x82, 0x80]
+    # non-finite poisons the block
+    codes, sc = oracle.mx_encode_f32(f32([1.0, np.inf, 2.0]), lib=lib)
+    assert sc[0] == 0xFF and np.all(codes == 0x7F)
+    # on bf16-representable values it agrees with the bf16 encoder
+    xb = (np.random.default_rng(2).standard_normal(32 * 40).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    a = oracle.mx_encode(xb, lib=lib)
+    b = oracle.mx_encode_f32(oracle.bf16_to_f32(xb), lib=lib)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+    # random fp32 blocks over many binades: each code is the nearest E4M3 value
+    # (ties to even) of x * 2^-e, with e from the block's amax
+    rng = np.random.default_rng(5)
+    x = (rng.standard_normal(32 * 300) * np.exp(rng.uniform(-30, 30, 32 * 300))).astype(np.float32)
+    x = x[:32 * 299 + 7]  # a ragged last block
+    codes, sc = oracle.mx_encode_f32(x, lib=lib)
+    for blk in range(sc.size):
+        v = x[32 * blk:32 * blk + 32].astype(np.float64)
+        k = np.frexp(np.max(np.abs(v)))[1]
+        e = int(np.clip(k - 1 - 8, -127, 127))
+        assert sc[blk] == e + 127
+        assert np.array_equal(codes[32 * blk:32 * blk + v.size], nearest_e4m3(np.ldexp(v, -e)))
+
+
 # ------------------------------------------------------------- sharding
 
 def pin_shard_layout(lib):
@@ -419,6 +458,7 @@ PINS = [
     pin_e4m3_encoder_exhaustive,
     pin_mx_scale_rule,
     pin_mx_loss_scale_shifts_scale_only,
+    pin_mx_f32_encoder,
     pin_shard_layout,
     pin_identical_learning,
     pin_resume,

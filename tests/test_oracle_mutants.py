@@ -43,9 +43,11 @@ MUTANTS = {
     "e4m3_bias_wrong": ("mag = (uint8_t)(((e + 7) << 3) + (r - 8));", "mag = (uint8_t)(((e + 8) << 3) + (r - 8));"),
     "e4m3_subnormal_step_wrong": ("mag = (uint8_t)round_half_even(a * 512.0);", "mag = (uint8_t)round_half_even(a * 256.0);"),
     "mx_scale_off_by_one": ("e = (k - 1) - emax_elem;", "e = k - emax_elem;"),
-    "mx_scale_not_clamped": ("            if (e < -127)\n                e = -127;\n", ""),
+    "mx_scale_not_clamped": ("        if (e < -127)\n            e = -127;\n", ""),
     "mx_nan_block_not_poisoned": ("nonfinite = 1;", "nonfinite = 0;"),
     "mx_decode_bias_wrong": ("return (float)ldexp(v, (int)scale - 127);", "return (float)ldexp(v, (int)scale - 128);"),
+    "mx_f32_through_bf16": ("vals[j] = (double)x[lo + j];",
+                            "vals[j] = (double)orc_bf16_to_f32(orc_f32_to_bf16(x[lo + j]));"),
     "shard_not_block_aligned": ("return (s + 31) / 32 * 32;", "return s;"),
     "running_power_reset": ("    ctr->b1p = 1.0;\n    ctr->b2p = 1.0;\n    for (int64_t k = 0; k < t; ++k) {",
                             "    ctr->b1p = 1.0;\n    ctr->b2p = 1.0;\n    for (int64_t k = 1; k < t; ++k) {"),
