@@ -361,6 +361,8 @@ def bench_ours(args, rank: int, world: int, local: int) -> dict | None:
     host_t = [torch.from_numpy(h.view(np.int16)).view(torch.bfloat16) for h in host]
     dev = [h.cuda() for h in host_t]
     opt = zb.ShardedAdamW(n, p, zb.Hparams(), torch.from_numpy(synth.init_weights(wl)), offload=args.offload)
+    if args.params == "mxfp8":
+        opt.use_mx_params()
     if args.variant == "staged":
         opt.use_staged()
     else:
@@ -432,6 +434,10 @@ def bench_ours(args, rank: int, world: int, local: int) -> dict | None:
         b_step = accounting.staged_shard_step_bytes_per_param() * n
         b_norm = accounting.staged_grad_norm_bytes_per_param(p) * n
         b_quant = 0.0
+    elif args.params == "mxfp8":
+        b_step = accounting.mx_params_shard_step_bytes_per_param(p) * n
+        b_norm = accounting.grad_norm_bytes_per_param(p) * n
+        b_quant = 0.0
     else:
         b_step = accounting.shard_step_bytes_per_param(p) * n
         b_norm = accounting.grad_norm_bytes_per_param(p) * n
@@ -500,8 +506,11 @@ def bench_ours(args, rank: int, world: int, local: int) -> dict | None:
     overlap = time_overlap(opt, wl, dev, stream, max(3, min(K, 50))) if args.overlap and not wl.mx else None
     step_kernel = ("zg_shard_step_mxfp8" if wl.mx else
                    "zg_shard_step_staged" if args.variant == "staged" else "zg_shard_step")
+    if args.params == "mxfp8":
+        step_kernel += "_mxparams"
     alternatives = {}
-    if not wl.mx and args.variant == "ldg" and not args.no_alternatives and not args.offload:
+    if (not wl.mx and args.variant == "ldg" and not args.no_alternatives and not args.offload
+            and args.params == "bf16"):
         for name in ("staged", "tma"):
             alternatives[name] = time_variant(name, wl, dev, stream, args.warmup, K, world)
     traffic = recorded_traffic(step_kernel, args.workload)
@@ -512,6 +521,7 @@ def bench_ours(args, rank: int, world: int, local: int) -> dict | None:
         "config": {"workload": args.workload if not args.n else f"{args.workload} with N={n}", "N": n, "P": p,
                    "loss_scale": ls, "variant": args.variant,
                    "optimizer_state": "pinned host memory (offloaded)" if args.offload else "HBM",
+                   "params": args.params,
                    "optimizer": "AdamW lr 1e-3 b 0.9/0.999 eps 1e-8 wd 0.01 clip 1.0",
                    "l2": f"inputs larger than L2: {(total * 2 * p + n * 14) / 1e9:.2f} GB working set vs 0.129 GB L2, no flush"},
         "roofline": {"bound": "hbm", "kernel": step_kernel, "achieved": achieved, "peak": peak,
@@ -573,6 +583,8 @@ def main(argv=None) -> int:
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-alternatives", action="store_true", help="skip timing the other bf16 variants")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end leg (very large workloads)")
+    ap.add_argument("--params", choices=["bf16", "mxfp8"], default="bf16",
+                    help="store the updated parameters as bf16 (default) or MXFP8 codes + scales")
     ap.add_argument("--overlap", action="store_true",
                     help="also time the bucketed norm overlapped with a stand-in backward pass")
     ap.add_argument("--offload", action="store_true",

@@ -185,6 +185,20 @@ int zg_get_info(zg_ctx *ctx, zg_stream stream, zg_step_info *info);
  * Synchronises the device; no step may be in flight on this context. */
 int zg_set_step(zg_ctx *ctx, int64_t t);
 
+/* Store the updated parameters as MXFP8 instead of bf16 (Zero From Scratch,
+ * item 14: MXFP8 takes its share off stored state; bf16 parameters and
+ * gradients as MXFP8 make a weight 16 - 2 * (2 - 33/32) bytes, 12 % less).
+ * After this call every step encodes the new fp32 master weights block by
+ * block with the rule of zg_quant_mxfp8 (E4M3 codes, one E8M0 scale per 32
+ * elements, round to nearest even, saturating; a short last block counts
+ * its missing elements as zero) and writes codes (N bytes, 16-byte aligned)
+ * and scales (ceil(N/32) bytes), caller-owned device memory, in place of the
+ * bf16 parameter buffer, which is then left untouched. The step pass moves
+ * 2P + 24 + 33/32 bytes per parameter instead of 2P + 26. Both pointers NULL
+ * goes back to bf16 parameters. Works with the plain and staged step
+ * kernels and the MX gradient path; refused with ZG_VARIANT_TMA. */
+int zg_bind_params_mxfp8(zg_ctx *ctx, uint8_t *codes, uint8_t *scales);
+
 /* The staged variant keeps the reduce-scatter output the way a stage-two
  * rank holds it (Zero From Scratch, item 7: the reduce-scatter leaves each
  * rank its summed shard): the norm pass writes the unscaled, averaged fp32

@@ -123,6 +123,11 @@ def staged_shard_step_bytes_per_param() -> int:
     return 4 + 2 * OPTIMIZER_STATE + PARAM_BF16
 
 
+def mx_params_shard_step_bytes_per_param(p: int) -> float:
+    """Fused step writing MXFP8 parameters (code + scale share) instead of bf16."""
+    return GRAD_BF16 * p + 2 * OPTIMIZER_STATE + MX_BYTES_PER_ELEMENT
+
+
 def mx_quant_bytes_per_param() -> float:
     """Encoding one rank's bf16 gradient: bf16 read, code + scale share written."""
     return GRAD_BF16 + MX_BYTES_PER_ELEMENT

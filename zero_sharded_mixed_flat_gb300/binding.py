@@ -95,6 +95,7 @@ def lib() -> ctypes.CDLL:
             "zg_shard_len": (_I64, [_P]),
             "zg_bind": (ctypes.c_int, [_P, _P, _P, _P, _P]),
             "zg_bind_grad_stage": (ctypes.c_int, [_P, _P]),
+            "zg_bind_params_mxfp8": (ctypes.c_int, [_P, _P, _P]),
             "zg_step": (ctypes.c_int, [_P, _P, ctypes.c_float, _P]),
             "zg_grad_norm": (ctypes.c_int, [_P, _P, ctypes.c_float, _P]),
             "zg_shard_step": (ctypes.c_int, [_P, _P, ctypes.c_float, _P]),
@@ -189,6 +190,18 @@ def zg_bind(ctx: Ctx, w: torch.Tensor, m: torch.Tensor, v: torch.Tensor, params:
 def zg_bind_grad_stage(ctx: Ctx, stage: torch.Tensor) -> None:
     _check(lib().zg_bind_grad_stage(ctx.handle, _dev_ptr(stage, torch.float32, ctx.n, "stage")), "zg_bind_grad_stage")
     ctx._stage = stage
+
+
+def zg_bind_params_mxfp8(ctx: Ctx, codes: torch.Tensor | None, scales: torch.Tensor | None) -> None:
+    """Write the parameters as MXFP8 codes + scales instead of bf16 (None, None: back to bf16)."""
+    if codes is None and scales is None:
+        _check(lib().zg_bind_params_mxfp8(ctx.handle, None, None), "zg_bind_params_mxfp8")
+        ctx._mx_params = None
+        return
+    c = _dev_ptr(codes, torch.uint8, ctx.n, "codes")
+    s = _dev_ptr(scales, torch.uint8, (ctx.n + 31) // 32, "scales")
+    _check(lib().zg_bind_params_mxfp8(ctx.handle, c, s), "zg_bind_params_mxfp8")
+    ctx._mx_params = (codes, scales)
 
 
 def _grads(ctx: Ctx, grads) -> ctypes.Array:
@@ -311,6 +324,13 @@ class ShardedAdamW:
         self.v = state()
         self.params = self.w.to(device=device, dtype=torch.bfloat16)
         zg_bind(self.ctx, self.w, self.m, self.v, self.params)
+
+    def use_mx_params(self) -> None:
+        """Store the parameters as MXFP8 (allocates codes and scales with torch)."""
+        dev = self.params.device
+        self.pcodes = torch.zeros(self.n, dtype=torch.uint8, device=dev)
+        self.pscales = torch.zeros((self.n + 31) // 32, dtype=torch.uint8, device=dev)
+        zg_bind_params_mxfp8(self.ctx, self.pcodes, self.pscales)
 
     def use_staged(self) -> None:
         """Switch to the staged variant (allocates the fp32 stage with torch)."""

@@ -26,6 +26,8 @@ struct zg_ctx {
     uint16_t *params;
     bool bound;
     float *stage;  // caller's fp32 buffer for the staged variant, or NULL
+    uint8_t *pcodes;      // MX parameter codes (written instead of bf16 params), or NULL
+    uint8_t *pscales;     // their E8M0 scales
     int64_t bucket_next;  // where the next bucket of an open bucketed norm must start
     bool bucket_open;     // a bucketed norm has started and not yet seen its last bucket
     int device;
@@ -91,7 +93,10 @@ float inv_scale(const zg_ctx *ctx, float loss_scale)
     return float(1.0 / denom);
 }
 
-zg::State state_of(const zg_ctx *ctx) { return zg::State{ctx->w, ctx->m, ctx->v, ctx->params}; }
+zg::State state_of(const zg_ctx *ctx)
+{
+    return zg::State{ctx->w, ctx->m, ctx->v, ctx->params, ctx->pcodes, ctx->pscales};
+}
 
 int finish_launch(cudaError_t e, const char *what) { return e == cudaSuccess ? ZG_OK : cuda_fail(e, what); }
 
@@ -207,6 +212,23 @@ int zg_bind(zg_ctx *ctx, float *w, float *m, float *v, uint16_t *params_bf16)
     ctx->v = v;
     ctx->params = params_bf16;
     ctx->bound = true;
+    return ZG_OK;
+}
+
+int zg_bind_params_mxfp8(zg_ctx *ctx, uint8_t *codes, uint8_t *scales)
+{
+    if (int rc = check_ctx(ctx, false)) return rc;
+    if (!codes && !scales) {
+        ctx->pcodes = nullptr;
+        ctx->pscales = nullptr;
+        return ZG_OK;
+    }
+    if (!codes || !scales) return fail(ZG_ERR_INVALID_ARG, "codes and scales must both be set (or both NULL)");
+    if (!aligned16(codes)) return fail(ZG_ERR_MISALIGNED, "codes must be 16-byte aligned");
+    if (ctx->variant == ZG_VARIANT_TMA)
+        return fail(ZG_ERR_INVALID_ARG, "MX parameters are written by the plain and staged step kernels, not the TMA one");
+    ctx->pcodes = codes;
+    ctx->pscales = scales;
     return ZG_OK;
 }
 
@@ -379,6 +401,8 @@ int zg_set_variant(zg_ctx *ctx, int variant)
     if (int rc = check_ctx(ctx, false)) return rc;
     if (variant != ZG_VARIANT_LDG && variant != ZG_VARIANT_TMA && variant != ZG_VARIANT_STAGED)
         return fail(ZG_ERR_INVALID_ARG, "unknown variant %d", variant);
+    if (variant == ZG_VARIANT_TMA && ctx->pcodes)
+        return fail(ZG_ERR_INVALID_ARG, "the TMA step kernel writes bf16 parameters only (MX parameters are bound)");
     if (variant == ZG_VARIANT_STAGED && !ctx->stage)
         return fail(ZG_ERR_NOT_BOUND, "the staged variant needs zg_bind_grad_stage first");
     ctx->variant = variant;

@@ -74,7 +74,9 @@ struct StepK {
 
 struct State {
     float *w, *m, *v;
-    uint16_t *p;
+    uint16_t *p;        // bf16 parameters (written unless MX parameters are bound)
+    uint8_t *pcodes;    // MXFP8 parameters: E4M3 codes, one per element, or null
+    uint8_t *pscales;   // and their E8M0 scales, one per 32 elements
 };
 
 constexpr int kStatusTimeout = -5;     // ZG_ERR_DEVICE_TIMEOUT
@@ -608,16 +610,25 @@ __device__ __forceinline__ void step_load(const Src &src, int64_t vec, const Sta
 }
 
 template <class Src>
-__device__ __forceinline__ void step_compute_store(const Src &src, int64_t vec, const VecData<Src> &d, float inv,
-                                                   float c, float bc1, float bc2, const StepK &k, const State &st)
+__device__ __forceinline__ void step_compute(const Src &src, const VecData<Src> &d, float inv, float c, float bc1,
+                                             float bc2, const StepK &k, float (&w)[kVec], float (&m)[kVec],
+                                             float (&v)[kVec])
 {
     float gh[kVec];
     src.reduce(d.raw, gh);
-    float w[kVec] = {d.w[0].x, d.w[0].y, d.w[0].z, d.w[0].w, d.w[1].x, d.w[1].y, d.w[1].z, d.w[1].w};
-    float m[kVec] = {d.m[0].x, d.m[0].y, d.m[0].z, d.m[0].w, d.m[1].x, d.m[1].y, d.m[1].z, d.m[1].w};
-    float v[kVec] = {d.v[0].x, d.v[0].y, d.v[0].z, d.v[0].w, d.v[1].x, d.v[1].y, d.v[1].z, d.v[1].w};
+    w[0] = d.w[0].x, w[1] = d.w[0].y, w[2] = d.w[0].z, w[3] = d.w[0].w;
+    w[4] = d.w[1].x, w[5] = d.w[1].y, w[6] = d.w[1].z, w[7] = d.w[1].w;
+    m[0] = d.m[0].x, m[1] = d.m[0].y, m[2] = d.m[0].z, m[3] = d.m[0].w;
+    m[4] = d.m[1].x, m[5] = d.m[1].y, m[6] = d.m[1].z, m[7] = d.m[1].w;
+    v[0] = d.v[0].x, v[1] = d.v[0].y, v[2] = d.v[0].z, v[3] = d.v[0].w;
+    v[4] = d.v[1].x, v[5] = d.v[1].y, v[6] = d.v[1].z, v[7] = d.v[1].w;
 #pragma unroll
     for (int j = 0; j < kVec; ++j) adamw(__fmul_rn(gh[j], inv), c, bc1, bc2, k, w[j], m[j], v[j]);
+}
+
+__device__ __forceinline__ void store_state(int64_t vec, const State &st, const float (&w)[kVec],
+                                            const float (&m)[kVec], const float (&v)[kVec])
+{
     float4 *w4 = reinterpret_cast<float4 *>(st.w) + 2 * vec;
     float4 *m4 = reinterpret_cast<float4 *>(st.m) + 2 * vec;
     float4 *v4 = reinterpret_cast<float4 *>(st.v) + 2 * vec;
@@ -627,9 +638,89 @@ __device__ __forceinline__ void step_compute_store(const Src &src, int64_t vec, 
     st_stream(m4 + 1, make_float4(m[4], m[5], m[6], m[7]));
     st_stream(v4, make_float4(v[0], v[1], v[2], v[3]));
     st_stream(v4 + 1, make_float4(v[4], v[5], v[6], v[7]));
+}
+
+template <class Src>
+__device__ __forceinline__ void step_compute_store(const Src &src, int64_t vec, const VecData<Src> &d, float inv,
+                                                   float c, float bc1, float bc2, const StepK &k, const State &st)
+{
+    float w[kVec], m[kVec], v[kVec];
+    step_compute(src, d, inv, c, bc1, bc2, k, w, m, v);
+    store_state(vec, st, w, m, v);
     st_stream(reinterpret_cast<uint4 *>(st.p) + vec,
               make_uint4(pack_bf16x2(w[0], w[1]), pack_bf16x2(w[2], w[3]), pack_bf16x2(w[4], w[5]),
                          pack_bf16x2(w[6], w[7])));
+}
+
+// ------------------------------------------------------------------ MXFP8 parameters
+//
+// The updated master weights stored as MXFP8 instead of bf16 (Zero From
+// Scratch, item 14: MXFP8 takes its share off stored state). Same block rule
+// as the gradient encoder, on fp32 values: amax over the |w| bit patterns,
+// E8M0 byte = max(E - 8, 0) from the amax exponent field E, codes =
+// E4M3(w * 2^-e) with round-to-nearest-even and saturation (the scaling is
+// exact whenever the code is not zero); a block with inf or NaN gets scale
+// 0xFF and codes 0x7F.
+
+__device__ __forceinline__ uint32_t mx_block_byte(uint32_t amax_bits, bool &bad)
+{
+    bad = amax_bits >= 0x7f800000u;
+    const uint32_t ex = amax_bits >> 23;
+    return bad ? 0xffu : (ex > 8u ? ex - 8u : 0u);
+}
+
+__device__ __forceinline__ float mx_to_unit(uint32_t sbyte, bool bad)
+{
+    return __uint_as_float((254u - (bad ? 0u : sbyte)) << 23);  // 2^-e
+}
+
+// Four consecutive lanes hold one 32-element block (8 values each): combine
+// their amax, then write this lane's 8 codes and (first lane) the scale.
+__device__ __forceinline__ void mx_store_group(int64_t vec, bool active, const float (&w)[kVec], const State &st)
+{
+    uint32_t amax = 0u;
+    if (active) {
+#pragma unroll
+        for (int j = 0; j < kVec; ++j) amax = max(amax, __float_as_uint(w[j]) & 0x7fffffffu);
+    }
+    amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    bool bad;
+    const uint32_t sbyte = mx_block_byte(amax, bad);
+    const float to_unit = mx_to_unit(sbyte, bad);
+    if (!active) return;
+    uint32_t pairs[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+        pairs[q] = bad ? 0x7f7fu : f32x2_to_e4m3x2(__fmul_rn(w[2 * q], to_unit), __fmul_rn(w[2 * q + 1], to_unit));
+    __stcs(reinterpret_cast<uint2 *>(st.pcodes) + vec, make_uint2(pairs[0] | (pairs[1] << 16), pairs[2] | (pairs[3] << 16)));
+    if ((threadIdx.x & 3) == 0) st.pscales[vec >> 2] = uint8_t(sbyte);
+}
+
+// The elements past the last whole 32-block, with MX parameters: update
+// them one by one, then encode the short block (missing elements count as
+// zero in its amax). One thread.
+template <class Src>
+__device__ __forceinline__ void step_tail_mx(const Src &src, int64_t n, float inv, float c, float bc1, float bc2,
+                                             const StepK &k, const State &st)
+{
+    const int64_t lo = (n / 32) * 32;
+    if (lo == n) return;
+    uint32_t amax = 0u;
+    for (int64_t i = lo; i < n; ++i) {
+        float w = st.w[i], m = st.m[i], v = st.v[i];
+        adamw(__fmul_rn(src.sum1(i), inv), c, bc1, bc2, k, w, m, v);
+        st.w[i] = w;
+        st.m[i] = m;
+        st.v[i] = v;
+        amax = max(amax, __float_as_uint(w) & 0x7fffffffu);
+    }
+    bool bad;
+    const uint32_t sbyte = mx_block_byte(amax, bad);
+    const float to_unit = mx_to_unit(sbyte, bad);
+    for (int64_t i = lo; i < n; ++i)
+        st.pcodes[i] = bad ? uint8_t(0x7f) : uint8_t(f32x2_to_e4m3x2(__fmul_rn(st.w[i], to_unit), 0.0f));
+    st.pscales[lo / 32] = uint8_t(sbyte);
 }
 
 template <class Src>
@@ -648,7 +739,7 @@ __device__ __forceinline__ void step_tail(const Src &src, int64_t n, float inv, 
 
 // Fused reduce-scatter + unscale + clip + AdamW + bf16 all-gather, one pass,
 // plain 128-bit loads and stores, grid-stride over 8-element vectors.
-template <class Src>
+template <class Src, bool kMxOut = false>
 __global__ void __launch_bounds__(kStepThreads, StepMinBlocks<Src>::value)
     step_kernel(Src src, int64_t n, float inv, StepK k, State st, Scalars *sc)
 {
@@ -668,7 +759,26 @@ __global__ void __launch_bounds__(kStepThreads, StepMinBlocks<Src>::value)
     pdl_trigger();
     float c, bc1, bc2;
     const int skip = step_prologue(sc, c, bc1, bc2);
-    if (skip == 0) {
+    if (skip == 0 && kMxOut) {
+        // whole 32-blocks: a warp-uniform loop so four lanes can share a block
+        const int64_t nvec = (n / 32) * 4;
+        const int64_t stride = int64_t(gridDim.x) * kStepThreads;
+        const int lane = threadIdx.x & 31;
+#pragma unroll 1
+        for (int64_t base = int64_t(blockIdx.x) * kStepThreads + (threadIdx.x & ~31); base < nvec; base += stride) {
+            const int64_t v = base + lane;
+            const bool active = v < nvec;
+            float w[kVec] = {}, m[kVec], vv[kVec];
+            if (active) {
+                VecData<Src> d;
+                step_load(src, v, st, d);
+                step_compute(src, d, inv, c, bc1, bc2, k, w, m, vv);
+                store_state(v, st, w, m, vv);
+            }
+            mx_store_group(v, active, w, st);
+        }
+        if (blockIdx.x == 0 && threadIdx.x == 0) step_tail_mx(src, n, inv, c, bc1, bc2, k, st);
+    } else if (skip == 0) {
         const int64_t nvec = n / kVec;
         const int64_t stride = int64_t(gridDim.x) * kStepThreads;
         constexpr int U = StepUnroll<Src>::value;

@@ -28,6 +28,20 @@ cudaError_t launch_step_mx(int p, const uint8_t *const *c, const uint8_t *const 
 cudaError_t launch_quant(const uint16_t *in, int64_t n, uint8_t *codes, uint8_t *scales, cudaStream_t st);
 cudaError_t launch_copy(const void *src, void *dst, int64_t bytes, cudaStream_t st);
 
+// Launch the step pass for one gradient source: grid = enough blocks for the
+// 8-element vectors, at most one wave; the MX-parameter instantiation when
+// the state carries MX parameter buffers.
+template <class Src>
+cudaError_t launch_step_kernel(const Src &src, int64_t n, float inv, StepK k, State state, Scalars *sc,
+                               cudaStream_t st)
+{
+    auto *kernel = state.pcodes ? &step_kernel<Src, true> : &step_kernel<Src, false>;
+    const int64_t want = (n / kVec + kStepThreads - 1) / kStepThreads;
+    const int wave = wave_blocks(reinterpret_cast<const void *>(kernel), kStepThreads, 0);
+    const int blocks = int(want < 1 ? 1 : (want < wave ? want : wave));
+    return launch_dependent(kernel, blocks, kStepThreads, 0, st, src, n, inv, k, state, sc);
+}
+
 // Largest grid any norm launch may use (sizes the partials array).
 int norm_blocks_cap();
 

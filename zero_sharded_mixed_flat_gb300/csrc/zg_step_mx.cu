@@ -13,11 +13,7 @@ cudaError_t launch_step_mx(int p, const uint8_t *const *c, const uint8_t *const 
             src.c[r] = c[r];
             src.s[r] = s[r];
         }
-        const void *fn = reinterpret_cast<const void *>(&step_kernel<MxSrc<P>>);
-        const int64_t want = (n / kVec + kStepThreads - 1) / kStepThreads;
-        const int wave = wave_blocks(fn, kStepThreads, 0);
-        const int blocks = int(want < 1 ? 1 : (want < wave ? want : wave));
-        return launch_dependent(&step_kernel<MxSrc<P>>, blocks, kStepThreads, 0, st, src, n, inv, k, state, sc);
+        return launch_step_kernel(src, n, inv, k, state, sc, st);
     });
 }
 
