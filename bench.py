@@ -304,6 +304,38 @@ def time_overlap(opt, wl, dev, stream, K: int, gemm_n: int = 8192) -> dict:
             "optimizer_exposed_serial_ms": t_serial - t_bwd, "optimizer_exposed_overlapped_ms": t_overlap - t_bwd}
 
 
+# --------------------------------------------------------------------- CUDA graphs
+
+def time_graph(opt, dev, ls, K: int, per_graph: int = 10) -> dict:
+    """The same steps captured `per_graph` at a time into one CUDA graph and
+    replayed: what launch overhead the eager loop still pays."""
+    import torch
+
+    side = torch.cuda.Stream()
+    with torch.cuda.stream(side):
+        opt.step(dev, ls, side)  # launch configurations cached before capture
+    side.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=side):
+        for _ in range(per_graph):
+            opt.step(dev, ls)
+    reps = max(1, K // per_graph)
+    for _ in range(2):
+        g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / (reps * per_graph)
+    info = opt.info()
+    assert info.status == 0 and not info.found_inf
+    return {"value": opt.n / (ms / 1e3), "unit": UNIT, "ms_per_step": ms, "steps_per_graph": per_graph,
+            "steps": reps * per_graph}
+
+
 # --------------------------------------------------------------------- our arm
 
 def time_variant(name: str, wl, dev, stream, warmup: int, K: int, world: int) -> dict:
@@ -504,6 +536,8 @@ def bench_ours(args, rank: int, world: int, local: int) -> dict | None:
     del src, dst
 
     overlap = time_overlap(opt, wl, dev, stream, max(3, min(K, 50))) if args.overlap and not wl.mx else None
+    graph = (time_graph(opt, dev, ls, K) if not wl.mx and args.variant == "ldg" and not args.offload
+             and args.params == "bf16" and not args.no_alternatives and world == 1 else None)
     step_kernel = ("zg_shard_step_mxfp8" if wl.mx else
                    "zg_shard_step_staged" if args.variant == "staged" else "zg_shard_step")
     if args.params == "mxfp8":
@@ -536,6 +570,7 @@ def bench_ours(args, rank: int, world: int, local: int) -> dict | None:
         "e2e": e2e,
         "alternatives": alternatives,
         **({"overlap": overlap} if overlap else {}),
+        **({"graph": graph} if graph else {}),
         "gpu_launches": (2 + (p if wl.mx else 0)) * K,
         "clocks": clk,
         "wall_s": wall,
