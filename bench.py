@@ -16,7 +16,9 @@ Prints one JSON line (rank 0). ``value`` is parameters updated per second
 over the whole job; ``roofline`` describes the fused shard-step kernel
 against the measured HBM bandwidth; ``e2e`` is the same metric through the
 C ABI with the gradients copied from pinned host memory every step and the
-step scalars read back; ``cpu_baseline`` is the oracle timed on the host.
+step scalars read back every step (step k+1's copy overlapped with step k
+through two device input slots; ``e2e.serial`` without that overlap);
+``cpu_baseline`` is the oracle timed on the host.
 
 Under torchrun (N > 1) every GPU runs its own independent P-rank problem (no
 collective on the data path: the simulated ranks live inside one GPU), so
@@ -336,6 +338,67 @@ def time_graph(opt, dev, ls, K: int, per_graph: int = 10) -> dict:
             "steps": reps * per_graph}
 
 
+# --------------------------------------------------------------------- end to end
+
+def time_e2e(h_in, slot_inputs, step_on, opt, stream, steps: int, world: int) -> dict:
+    """Steps fed from pinned host memory, each step's result read back.
+
+    Serial: copy a step's inputs, run the step, read its result, in turn.
+    Pipelined (a caller's double buffer): two device slots; step k+1's inputs
+    are copied on a second stream while step k runs, and a slot is refilled
+    only after the step that read it is done. Both timed regions hold every
+    step's copy and every step's result read."""
+    import torch
+
+    copy_stream = torch.cuda.Stream()
+    copied = [torch.cuda.Event(), torch.cuda.Event()]
+    consumed = [torch.cuda.Event(), torch.cuda.Event()]
+
+    def feed(k):
+        with torch.cuda.stream(copy_stream):
+            copy_stream.wait_event(consumed[k])
+            for d, h in zip(slot_inputs(k), h_in):
+                d.copy_(h, non_blocking=True)
+            copied[k].record(copy_stream)
+
+    def serial(count):
+        for _ in range(count):
+            for d, h in zip(slot_inputs(0), h_in):
+                d.copy_(h, non_blocking=True)
+            step_on(0)
+            opt.info(stream)  # device->host read of the step result; synchronises
+
+    def pipelined(count):
+        copy_stream.wait_stream(stream)
+        feed(0)
+        for k in range(count):
+            s = k % 2
+            stream.wait_event(copied[s])
+            step_on(s)
+            consumed[s].record(stream)
+            if k + 1 < count:
+                feed(1 - s)
+            opt.info(stream)
+
+    def timed(run):
+        run(2)
+        barrier(world)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        run(steps)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return max_over_ranks(e0.elapsed_time(e1) / 1e3, world) / steps
+
+    s_serial = timed(serial)
+    s_pipe = timed(pipelined)
+    info = opt.info(stream)
+    assert info.status == 0 and not info.found_inf
+    return {"s_per_step": s_pipe, "serial_s_per_step": s_serial, "steps": steps,
+            "pipeline": "two device input slots; step k+1's inputs copied on a second stream during step k"}
+
+
 # --------------------------------------------------------------------- our arm
 
 def time_variant(name: str, wl, dev, stream, warmup: int, K: int, world: int) -> dict:
@@ -492,45 +555,36 @@ def bench_ours(args, rank: int, world: int, local: int) -> dict | None:
     # path's inputs are the P bf16 gradient buffers; the MX path's inputs are
     # the encoded wire payload, codes and scales (encoded once on the GPU
     # here and parked in host memory, as a sending rank would transmit them).
-    if args.no_e2e:
-        pass
-    elif wl.mx:
-        for r in range(p):
-            zb.zg_quant_mxfp8(dev[r], codes[r], scales[r], n, stream)
-        h_in = [c[:n].cpu().pin_memory() for c in codes] + [sc[:(n + 31) // 32].cpu().pin_memory() for sc in scales]
-        d_in = [c[:n] for c in codes] + [sc[:(n + 31) // 32] for sc in scales]
+    e2e = None
+    if not args.no_e2e:
+        if wl.mx:
+            for r in range(p):
+                zb.zg_quant_mxfp8(dev[r], codes[r], scales[r], n, stream)
+            slots = [(codes, scales),
+                     ([torch.empty_like(c) for c in codes], [torch.empty_like(s) for s in scales])]
+            h_in = [c[:n].cpu().pin_memory() for c in codes] + [s[:(n + 31) // 32].cpu().pin_memory() for s in scales]
 
-        def e2e_step():
-            for d, h in zip(d_in, h_in):
-                d.copy_(h, non_blocking=True)
-            zb.zg_step_mxfp8(opt.ctx, codes, scales, ls, stream)
-            opt.info(stream)  # device->host read of the step result; synchronises
-    else:
-        h_in = [h.pin_memory() for h in host_t]
-        d_in = dev
+            def slot_inputs(k):
+                c, s = slots[k]
+                return [x[:n] for x in c] + [x[:(n + 31) // 32] for x in s]
 
-        def e2e_step():
-            for d, h in zip(d_in, h_in):
-                d.copy_(h, non_blocking=True)
-            run_step()
-            opt.info(stream)  # device->host read of the step result; synchronises
-    e2e_steps = max(3, min(K, 200))
-    for _ in range(0 if args.no_e2e else 2):
-        e2e_step()
-    barrier(world)
-    torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(0 if args.no_e2e else e2e_steps):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_s = max_over_ranks(e0.elapsed_time(e1) / 1e3, world)
-    e2e = None if args.no_e2e else {"value": world * n * e2e_steps / e2e_s, "unit": UNIT, "steps": e2e_steps,
-           "h2d_bytes_per_step": sum(h.numel() * h.element_size() for h in h_in),
-           "d2h_bytes_per_step": SCALARS_D2H_BYTES,
-           "inputs": "MXFP8 codes + scales (the wire payload)" if wl.mx else "P bf16 gradient buffers"}
+            def step_on(k):
+                zb.zg_step_mxfp8(opt.ctx, slots[k][0], slots[k][1], ls, stream)
+        else:
+            slots = [dev, [torch.empty_like(d) for d in dev]]
+            h_in = [h.pin_memory() for h in host_t]
+
+            def slot_inputs(k):
+                return slots[k]
+
+            def step_on(k):
+                zb.zg_step(opt.ctx, slots[k], ls, stream)
+        e2e = time_e2e(h_in, slot_inputs, step_on, opt, stream, max(3, min(K, 200)), world)
+        e2e.update(h2d_bytes_per_step=sum(h.numel() * h.element_size() for h in h_in),
+                   d2h_bytes_per_step=SCALARS_D2H_BYTES,
+                   inputs="MXFP8 codes + scales (the wire payload)" if wl.mx else "P bf16 gradient buffers")
+        e2e = {"value": world * n / e2e.pop("s_per_step"), "unit": UNIT,
+               "serial": world * n / e2e.pop("serial_s_per_step"), **e2e}
 
     # copy probe: achievable HBM bandwidth in the same process
     src = torch.empty(1 << 30, dtype=torch.uint8, device="cuda")
