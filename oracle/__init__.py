@@ -98,6 +98,8 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
         "orc_step_mx": (ctypes.c_int, [_I64, ctypes.c_int, _P, _P, ctypes.c_float, _P, _P, _P, _P, _P, _P, _P]),
         "orc_step_sharded": (ctypes.c_int, [_I64, ctypes.c_int, _P, ctypes.c_float, _P, _P, _P, _P, _P, _P, _P]),
         "orc_counters_at": (None, [_P, _I64, _P]),
+        "orc_gather": (None, [_I64, _P, _I64, _I64, _P]),
+        "orc_gather_mx": (None, [_I64, _P, _P, _I64, _I64, _P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -216,6 +218,28 @@ def mx_encode_f32(x: np.ndarray, lib=None):
 
 def mx_decode(code: int, scale: int, lib=None) -> float:
     return float((lib or load()).orc_mx_decode(int(code), int(scale)))
+
+
+def gather(shards, s: int, lo: int, hi: int, lib=None) -> np.ndarray:
+    """Stage-three just-in-time gather of bf16 parameters [lo, hi) from the P
+    rank shards (each S long) (DeepSpeed documentation review, paragraph on
+    the three stages). Returns the bf16 patterns, uint16[hi - lo]."""
+    lib = lib or load()
+    shards = [np.ascontiguousarray(x, dtype=np.uint16) for x in shards]
+    out = np.zeros(max(hi - lo, 0), dtype=np.uint16)
+    lib.orc_gather(s, _ptr_array(shards), lo, hi, _ptr(out))
+    return out
+
+
+def gather_mx(codes, scales, s: int, lo: int, hi: int, lib=None) -> np.ndarray:
+    """The gather from MXFP8 parameter shards (codes S long, scales S/32),
+    decoded and rounded to bf16 (Zero From Scratch, item 14)."""
+    lib = lib or load()
+    codes = [np.ascontiguousarray(x, dtype=np.uint8) for x in codes]
+    scales = [np.ascontiguousarray(x, dtype=np.uint8) for x in scales]
+    out = np.zeros(max(hi - lo, 0), dtype=np.uint16)
+    lib.orc_gather_mx(s, _ptr_array(codes), _ptr_array(scales), lo, hi, _ptr(out))
+    return out
 
 
 def inv_scale(loss_scale: float, p: int, grad_average: int = 1, lib=None) -> float:

@@ -480,3 +480,37 @@ void orc_counters_at(const orc_hparams *hp, int64_t t, orc_counters *ctr)
         ctr->b2p = ctr->b2p * hp->beta2;
     }
 }
+
+/* ------------------------------------------------------------------ */
+/* Stage three: parameters gathered just in time.                      */
+/* ------------------------------------------------------------------ */
+
+/* With the parameters themselves sharded (DeepSpeed documentation review,
+ * paragraph on the three stages; Zero From Scratch, items 9 and 18: the
+ * third flag), rank r keeps only the bf16 parameters [r*S, (r+1)*S), and a
+ * layer that computes on flat indices [lo, hi) first gathers them from
+ * their owners. Flat index i lives on rank i / S at offset i mod S.
+ * out[i - lo] receives that element for every i in [lo, hi). */
+void orc_gather(int64_t s, const uint16_t *const *shards, int64_t lo, int64_t hi, uint16_t *out)
+{
+    for (int64_t i = lo; i < hi; ++i) {
+        int64_t r = i / s;
+        int64_t k = i - r * s;
+        out[i - lo] = shards[r][k];
+    }
+}
+
+/* The same gather from parameter shards stored as MXFP8 (Zero From Scratch,
+ * item 14: MXFP8 on stored state): each gathered element is decoded to its
+ * exact binary32 value and rounded to bf16 for the layer's computation. A
+ * decoded value has at most four significant bits, so the rounding changes
+ * nothing above the bf16 subnormal range; NaN gathers as NaN. */
+void orc_gather_mx(int64_t s, const uint8_t *const *codes, const uint8_t *const *scales,
+                   int64_t lo, int64_t hi, uint16_t *out)
+{
+    for (int64_t i = lo; i < hi; ++i) {
+        int64_t r = i / s;
+        int64_t k = i - r * s;
+        out[i - lo] = orc_f32_to_bf16(orc_mx_decode(codes[r][k], scales[r][k / 32]));
+    }
+}

@@ -22,7 +22,10 @@ What pins what:
   - the MX scale rule on blocks built by hand from the format;
   - shard layout invariants; identical learning (sharded == unsharded);
   - resume (set_step) reproduces an uninterrupted run;
-  - power-of-two loss-scale invariance of the whole step.
+  - power-of-two loss-scale invariance of the whole step;
+  - stage three's gather: shards holding their own flat indices read back as
+    the indices; MX shards built by hand from the formats and random ones
+    decoded through torch's float8 values and bf16 cast.
 """
 from __future__ import annotations
 
@@ -443,6 +446,77 @@ def pin_resume(lib):
     assert t == 10 and abs(b1p - 0.9 ** 10) <= 1e-15 and abs(b2p - 0.999 ** 10) <= 1e-15
 
 
+def _ranges(s: int, p: int):
+    """Gather ranges that start and end on, next to and away from shard edges."""
+    n = p * s
+    edges = sorted({0, 1, s - 1, s, s + 1, n // 2, n - s - 1, n - s, n - 1, n} & set(range(n + 1)))
+    return [(lo, hi) for lo in edges for hi in edges if hi >= lo]
+
+
+def pin_gather_owner_offset(lib):
+    """Stage three's gather (DeepSpeed documentation review, paragraph on the
+    stages): with every rank's shard holding its own flat indices as values,
+    a gathered range must read back as the indices themselves."""
+    for p, s in ((1, 32), (2, 32), (3, 64), (5, 32), (8, 96)):
+        shards = [np.arange(r * s, (r + 1) * s, dtype=np.uint16) for r in range(p)]
+        for lo, hi in _ranges(s, p):
+            got = oracle.gather(shards, s, lo, hi, lib=lib)
+            assert np.array_equal(got, np.arange(lo, hi, dtype=np.uint16)), (p, s, lo, hi)
+
+
+def pin_gather_mx_hand_values(lib):
+    """MX parameter shards built by hand from the formats: E4M3 (bias 7,
+    subnormals m/8 * 2^-6), E8M0 scale 2^(s - 127), bf16 with round to nearest
+    even, whose subnormal step is 2^-133."""
+    s = 96
+    codes = [np.zeros(s, np.uint8), np.zeros(s, np.uint8)]
+    scales = [np.array([119, 0, 127], np.uint8), np.array([120, 127, 0xFF], np.uint8)]
+    want = np.zeros(2 * s, np.uint16)
+    want[2 * s - 32:] = 0x7FC0  # a NaN scale: the whole block gathers as NaN
+    cases = [  # (rank, index in shard, code, expected bf16)
+        (0, 0, 0x78, 0x3F80),   # 256 * 2^-8 = 1
+        (0, 1, 0xF8, 0xBF80),   # -1
+        (0, 2, 0x80, 0x8000),   # -0 keeps its sign
+        (0, 3, 0x7F, 0x7FC0),   # NaN code
+        (0, 32, 0x05, 0x0001),  # 5 * 2^-136 = 0.625 subnormal steps -> 1
+        (0, 33, 0x04, 0x0000),  # 0.5 steps: tie to even -> 0
+        (0, 34, 0x0C, 0x0002),  # 1.5 * 2^-6 * 2^-127 = 1.5 steps: tie to even -> 2
+        (0, 35, 0x84, 0x8000),  # -0.5 steps -> -0
+        (1, 0, 0x78, 0x4000),   # 256 * 2^-7 = 2: rank one's own scale
+        (1, 32, 0x7E, 0x43E0),  # 448
+        (1, 33, 0x01, 0x3B00),  # 2^-9
+        (1, 34, 0xB9, 0xBF90),  # exponent field 7: -(1 + 1/8) * 2^0 = -1.125
+    ]
+    for r, k, c, b in cases:
+        codes[r][k] = c
+        want[r * s + k] = b
+    for lo, hi in _ranges(s, 2) + [(30, 40), (s - 3, s + 40)]:
+        got = oracle.gather_mx(codes, scales, s, lo, hi, lib=lib)
+        assert np.array_equal(got, want[lo:hi]), (lo, hi, got, want[lo:hi])
+
+
+def pin_gather_mx_vs_torch(lib):
+    """Random MX shards decoded through torch's float8_e4m3fn values, an
+    exact power-of-two scaling and torch's bf16 cast."""
+    import torch
+
+    rng = np.random.default_rng(23)
+    p, s = 3, 4096
+    codes, scales = [], []
+    for _ in range(p):
+        c = rng.integers(0, 256, s).astype(np.uint8)
+        c[(c & 0x7F) == 0x7F] = 0x3C  # no NaN codes here
+        codes.append(c)
+        scales.append(np.concatenate([rng.integers(100, 150, s // 32 - 8), rng.integers(0, 8, 8)]).astype(np.uint8))
+    flat_vals = []
+    for c, sc in zip(codes, scales):
+        v = torch.from_numpy(c).view(torch.float8_e4m3fn).float().numpy().astype(np.float64)
+        flat_vals.append(np.ldexp(v, np.repeat(sc.astype(np.int64) - 127, 32)).astype(np.float32))
+    ref = torch.from_numpy(np.concatenate(flat_vals)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    for lo, hi in ((0, p * s), (5, 4100), (4096, 8192), (8000, 12288)):
+        assert np.array_equal(oracle.gather_mx(codes, scales, s, lo, hi, lib=lib), ref[lo:hi]), (lo, hi)
+
+
 PINS = [
     pin_first_step_closed_form,
     pin_first_step_weight_decay,
@@ -462,6 +536,9 @@ PINS = [
     pin_shard_layout,
     pin_identical_learning,
     pin_resume,
+    pin_gather_owner_offset,
+    pin_gather_mx_hand_values,
+    pin_gather_mx_vs_torch,
 ]
 
 

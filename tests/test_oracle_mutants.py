@@ -49,6 +49,12 @@ MUTANTS = {
     "mx_f32_through_bf16": ("vals[j] = (double)x[lo + j];",
                             "vals[j] = (double)orc_bf16_to_f32(orc_f32_to_bf16(x[lo + j]));"),
     "shard_not_block_aligned": ("return (s + 31) / 32 * 32;", "return s;"),
+    "gather_neighbour_offset": ("out[i - lo] = shards[r][k];", "out[i - lo] = shards[r][k ^ 1];"),
+    "gather_from_rank_zero": ("out[i - lo] = shards[r][k];", "out[i - lo] = shards[0][k];"),
+    "gather_mx_scale_of_rank_zero": ("scales[r][k / 32]", "scales[0][k / 32]"),
+    "gather_mx_scale_per_64": ("scales[r][k / 32]", "scales[r][k / 64]"),
+    "gather_mx_truncates": ("out[i - lo] = orc_f32_to_bf16(orc_mx_decode(codes[r][k], scales[r][k / 32]));",
+                            "out[i - lo] = (uint16_t)(bits_from_f32(orc_mx_decode(codes[r][k], scales[r][k / 32])) >> 16);"),
     "running_power_reset": ("    ctr->b1p = 1.0;\n    ctr->b2p = 1.0;\n    for (int64_t k = 0; k < t; ++k) {",
                             "    ctr->b1p = 1.0;\n    ctr->b2p = 1.0;\n    for (int64_t k = 1; k < t; ++k) {"),
 }
