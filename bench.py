@@ -306,6 +306,136 @@ def time_overlap(opt, wl, dev, stream, K: int, gemm_n: int = 8192) -> dict:
             "optimizer_exposed_serial_ms": t_serial - t_bwd, "optimizer_exposed_overlapped_ms": t_overlap - t_bwd}
 
 
+# --------------------------------------------------------------------- stage three
+
+def stage3_layers(wl) -> list[tuple[int, int]]:
+    """Layer ranges [lo, hi) of the flat vector: for GPT-2 small its
+    embeddings, twelve blocks and final norm; otherwise 16 near-equal parts
+    cut at multiples of 768."""
+    from zero_sharded_mixed_flat_gb300 import synth
+
+    if wl.name == "gpt2small_p8" and wl.n == 124_439_808:
+        out, lo, key_prev = [], 0, None
+        for name, k in synth.gpt2_small_tensors():
+            key = "embed" if name in ("wte", "wpe") else name.split(".")[0]
+            if key == key_prev:
+                out[-1] = (out[-1][0], lo + k)
+            else:
+                out.append((lo, lo + k))
+            key_prev, lo = key, lo + k
+        return out
+    cuts = sorted({min(wl.n, round(i * wl.n / 16 / 768) * 768) for i in range(16)} | {wl.n})
+    return [(a, b) for a, b in zip(cuts[:-1], cuts[1:]) if b > a]
+
+
+def time_stage3(opt, wl, K: int, peak: float, tokens: int = 8192) -> dict:
+    """Stage three's just-in-time parameter gather over a forward sweep.
+
+    Gather alone: every layer's parameters gathered from the P shards, back
+    to back (the kernel's bandwidth). Forward stand-in: per layer one bf16
+    GEMM of [tokens x 768] by the gathered parameters viewed as [768 x k]
+    (2 * tokens flops per parameter, cuBLAS). Serial: gather, then GEMM, layer
+    by layer. Overlapped: layer i+1 is gathered on a second stream into the
+    other of two buffers while layer i's GEMM runs (that stream at high or at
+    equal priority). Each sweep is captured once in a CUDA graph and replayed,
+    as a per-layer loop runs in production, so host launch costs stay out of
+    the GPU times. Reported: per-sweep times and the gather time left exposed."""
+    import torch
+
+    from zero_sharded_mixed_flat_gb300 import accounting
+
+    layers = stage3_layers(wl)
+    d = 768
+    big = max(hi - lo for lo, hi in layers)
+    bufs = [torch.empty(big, dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    x = torch.randn(tokens, d, dtype=torch.bfloat16, device="cuda")
+    y = torch.empty(tokens * (big // d), dtype=torch.bfloat16, device="cuda")
+    side_hi = torch.cuda.Stream(priority=-1)  # gather blocks go first whenever GEMM blocks retire
+    side_eq = torch.cuda.Stream()
+    gathered = [torch.cuda.Event() for _ in layers]
+    used = [torch.cuda.Event(), torch.cuda.Event()]
+
+    def gather(i, b, st):
+        lo, hi = layers[i]
+        opt.gather(lo, hi, bufs[b][:hi - lo], st)
+
+    def compute(i, b):
+        lo, hi = layers[i]
+        k = (hi - lo) // d // 8 * 8  # an aligned leading dimension keeps cuBLAS on its tensor-core kernels
+        torch.matmul(x, bufs[b][:k * d].view(d, k), out=y[:tokens * k].view(tokens, k))
+
+    def gathers_only():
+        cur = torch.cuda.current_stream()
+        for i in range(len(layers)):
+            gather(i, i % 2, cur)
+
+    def gemms_only():
+        for i in range(len(layers)):
+            compute(i, i % 2)
+
+    def serial():
+        cur = torch.cuda.current_stream()
+        for i in range(len(layers)):
+            gather(i, i % 2, cur)
+            compute(i, i % 2)
+
+    def overlapped(side):
+        def run():
+            cur = torch.cuda.current_stream()
+            side.wait_stream(cur)
+            gather(0, 0, side)
+            gathered[0].record(side)
+            for i in range(len(layers)):
+                b = i % 2
+                if i + 1 < len(layers):
+                    if i >= 1:
+                        side.wait_event(used[1 - b])  # layer i-1's GEMM is done with that buffer
+                    gather(i + 1, 1 - b, side)
+                    gathered[i + 1].record(side)
+                cur.wait_event(gathered[i])
+                compute(i, b)
+                used[b].record(cur)
+        return run
+
+    def timed(fn):
+        fn()  # launch configurations cached before capture
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(K):
+            g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / K
+
+    mx = getattr(opt, "pcodes", None) is not None
+    t_gather = timed(gathers_only)
+    t_gemm = timed(gemms_only)
+    t_serial = timed(serial)
+    t_hi = timed(overlapped(side_hi))
+    t_eq = timed(overlapped(side_eq))
+    per_param = accounting.mx_gather_bytes_per_param() if mx else accounting.gather_bytes_per_param()
+    gbs = per_param * wl.n / (t_gather / 1e3) / 1e9
+    flops = 2 * tokens * sum((hi - lo) // d // 8 * 8 * d for lo, hi in layers)
+    return {"layers": len(layers), "largest_layer": big, "shards": "MXFP8 codes + scales" if mx else "bf16",
+            "timing": "each sweep captured in a CUDA graph, replayed",
+            "gather_ms": t_gather, "gather_gbs": gbs, "gather_frac": gbs / peak,
+            "gather_bytes_per_param": per_param,
+            "forward_stand_in": f"per layer one bf16 GEMM [{tokens} x {d}] x [{d} x layer/{d}] (cuBLAS)",
+            "gemm_ms": t_gemm, "gemm_tflops": flops / (t_gemm / 1e3) / 1e12,
+            "serial_ms": t_serial, "overlapped_ms": t_hi, "overlapped_equal_priority_ms": t_eq,
+            "gather_exposed_serial_ms": t_serial - t_gemm, "gather_exposed_overlapped_ms": t_hi - t_gemm,
+            "gather_exposed_overlapped_equal_priority_ms": t_eq - t_gemm,
+            "ring_bytes_per_rank_per_sweep": accounting.ring_bytes_sent_per_rank(
+                (accounting.MX_BYTES_PER_ELEMENT if mx else accounting.PARAM_BF16) * wl.n, wl.p, "all_gather")}
+
+
 # --------------------------------------------------------------------- CUDA graphs
 
 def time_graph(opt, dev, ls, K: int, per_graph: int = 10) -> dict:
@@ -601,6 +731,7 @@ def bench_ours(args, rank: int, world: int, local: int) -> dict | None:
     del src, dst
 
     overlap = time_overlap(opt, wl, dev, stream, max(3, min(K, 50))) if args.overlap and not wl.mx else None
+    stage3 = time_stage3(opt, wl, max(3, min(K, 20)), peak) if args.stage3 else None
     graph = (time_graph(opt, dev, ls, K) if not wl.mx and args.variant == "ldg" and not args.offload
              and args.params == "bf16" and not args.no_alternatives and world == 1 else None)
     step_kernel = ("zg_shard_step_mxfp8" if wl.mx else
@@ -636,6 +767,7 @@ def bench_ours(args, rank: int, world: int, local: int) -> dict | None:
         "e2e": e2e,
         "alternatives": alternatives,
         **({"overlap": overlap} if overlap else {}),
+        **({"stage3": stage3} if stage3 else {}),
         **({"graph": graph} if graph else {}),
         "gpu_launches": (2 + (p if wl.mx else 0)) * K,
         "clocks": clk,
@@ -688,6 +820,8 @@ def main(argv=None) -> int:
                     help="store the updated parameters as bf16 (default) or MXFP8 codes + scales")
     ap.add_argument("--overlap", action="store_true",
                     help="also time the bucketed norm overlapped with a stand-in backward pass")
+    ap.add_argument("--stage3", action="store_true",
+                    help="also time stage three's just-in-time parameter gather over a forward sweep")
     ap.add_argument("--offload", action="store_true",
                     help="fp32 optimizer state in pinned host memory, read and written over the host link")
     args = ap.parse_args(argv)

@@ -221,6 +221,37 @@ int zg_set_variant(zg_ctx *ctx, int variant);
  * (used to test that path). */
 int zg_set_wait_limit(zg_ctx *ctx, int64_t polls);
 
+/* Stage three: parameters gathered just in time (DeepSpeed documentation
+ * review, paragraph on the three stages: the parameters themselves are split,
+ * gathered for each layer's computation and released afterwards; Zero From
+ * Scratch, items 9 and 18, the third flag). Rank r keeps only the parameters
+ * [r*S, (r+1)*S) in shards[r], a device buffer of S = zg_shard_len(ctx) bf16
+ * values (the bf16 parameter vector zg_bind received is exactly these P
+ * shards end to end: shards[r] = params + r*S). The call writes the flat
+ * parameters [lo, hi), 0 <= lo <= hi <= N, into out[0, hi - lo): out[j] is
+ * element (lo + j) mod S of shard (lo + j) / S. On one GPU this stands for the
+ * all-gather every rank runs before the layer; `out` is the caller's
+ * (device) working buffer, which it releases or reuses after the layer.
+ * Every shards[r] and out must be 16-byte aligned device memory (else
+ * ZG_ERR_MISALIGNED); NULL pointers or a range outside [0, N) give
+ * ZG_ERR_INVALID_ARG; lo == hi does nothing. An lo that is a multiple of 8
+ * takes the vector path (one 16-byte load and store per 8 values). Moves 4
+ * bytes per gathered parameter. Stream-ordered, no allocation. */
+int zg_gather_params(const zg_ctx *ctx, const uint16_t *const *shards, int64_t lo, int64_t hi, uint16_t *out,
+                     zg_stream stream);
+
+/* The same gather from parameter shards stored as MXFP8 (Zero From Scratch,
+ * item 14: MXFP8 on stored state, the layout zg_bind_params_mxfp8 writes):
+ * codes[r] holds S E4M3 codes of rank r (16-byte aligned) and scales[r] its
+ * S/32 E8M0 scales. Each gathered element is decoded to its exact binary32
+ * value code * 2^(scale - 127) and rounded to bf16 (nearest even; this only
+ * acts below 2^-126, since a decoded value has at most four significant
+ * bits); a NaN code or scale gathers as 0x7FC0. An lo that is a multiple of
+ * 16 takes the vector path. Reads 1 + 1/32 and writes 2 bytes per gathered
+ * parameter. Errors as zg_gather_params. */
+int zg_gather_params_mxfp8(const zg_ctx *ctx, const uint8_t *const *codes, const uint8_t *const *scales, int64_t lo,
+                           int64_t hi, uint16_t *out, zg_stream stream);
+
 /* Measurement aid: copy `bytes` (a multiple of 16, both pointers 16-byte
  * aligned device memory) with a plain streaming copy kernel; its time gives
  * the achievable HBM bandwidth in the same run. */

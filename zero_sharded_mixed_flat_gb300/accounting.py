@@ -141,6 +141,16 @@ def mx_shard_step_bytes_per_param(p: int) -> float:
     return MX_BYTES_PER_ELEMENT * p + 2 * OPTIMIZER_STATE + PARAM_BF16
 
 
+def gather_bytes_per_param() -> int:
+    """Stage three's gather of one bf16 parameter: read from its shard, written out."""
+    return PARAM_BF16 + PARAM_BF16
+
+
+def mx_gather_bytes_per_param() -> float:
+    """The gather from MXFP8 shards: code + scale share read, bf16 written."""
+    return MX_BYTES_PER_ELEMENT + PARAM_BF16
+
+
 def resident_bytes(n_params: int, p: int, shard_len: int) -> dict:
     """Device bytes the single-GPU simulation of P ranks holds: fp32 w/m/v and
     bf16 params over P*S elements, and P bf16 gradient buffers of P*S each."""

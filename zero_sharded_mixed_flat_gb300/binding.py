@@ -109,6 +109,8 @@ def lib() -> ctypes.CDLL:
             "zg_set_variant": (ctypes.c_int, [_P, ctypes.c_int]),
             "zg_set_wait_limit": (ctypes.c_int, [_P, _I64]),
             "zg_probe_copy": (ctypes.c_int, [_P, _P, _I64, _P]),
+            "zg_gather_params": (ctypes.c_int, [_P, _P, _I64, _I64, _P, _P]),
+            "zg_gather_params_mxfp8": (ctypes.c_int, [_P, _P, _P, _I64, _I64, _P, _P]),
             "zg_grad_norm_noalloc": (ctypes.c_int, [_P, ctypes.c_int, _I64, ctypes.c_float, ctypes.c_int, _P, _P]),
             "zg_destroy": (None, [_P]),
             "zg_strerror": (ctypes.c_char_p, [ctypes.c_int]),
@@ -236,6 +238,38 @@ def zg_shard_step(ctx: Ctx, grads, loss_scale: float, stream=None) -> None:
     _check(lib().zg_shard_step(ctx.handle, _grads(ctx, grads), loss_scale, _stream(stream)), "zg_shard_step")
 
 
+def _shard_ptrs(ctx: Ctx, shards, dtype: torch.dtype, block: int, what: str) -> ctypes.Array:
+    """P shard pointers, one unit per ``block`` parameters (1 for values and
+    codes, 32 for MX scales): from P tensors (rank r's part), or from one
+    tensor holding all P shards end to end (rank r's part starts at unit
+    r * S / block; ranks that own nothing get a pointer that is never read)."""
+    s = zg_shard_len(ctx)
+    if isinstance(shards, torch.Tensor):
+        base = _dev_ptr(shards, dtype, -(-ctx.n // block), what)
+        return _ptr_array([base + r * (s // block) * shards.element_size() for r in range(ctx.p)])
+    if len(shards) != ctx.p:
+        raise ValueError(f"expected {ctx.p} {what} shards, got {len(shards)}")
+    need = [-(-max(0, min(s, ctx.n - r * s)) // block) for r in range(ctx.p)]
+    return _ptr_array([_dev_ptr(x, dtype, need[r], f"{what}[{r}]") for r, x in enumerate(shards)])
+
+
+def zg_gather_params(ctx: Ctx, shards, lo: int, hi: int, out: torch.Tensor, stream=None) -> None:
+    """Stage three: parameters [lo, hi) gathered from the P bf16 shards into
+    out[0, hi - lo). ``shards``: P tensors, or the whole parameter vector."""
+    sp = _shard_ptrs(ctx, shards, torch.bfloat16, 1, "shards")
+    o = _dev_ptr(out, torch.bfloat16, max(hi - lo, 0), "out")
+    _check(lib().zg_gather_params(ctx.handle, sp, lo, hi, o, _stream(stream)), "zg_gather_params")
+
+
+def zg_gather_params_mxfp8(ctx: Ctx, codes, scales, lo: int, hi: int, out: torch.Tensor, stream=None) -> None:
+    """The gather from MXFP8 parameter shards, decoded to bf16. ``codes`` and
+    ``scales``: P tensors each, or the whole code and scale vectors."""
+    cp = _shard_ptrs(ctx, codes, torch.uint8, 1, "codes")
+    sp = _shard_ptrs(ctx, scales, torch.uint8, 32, "scales")
+    o = _dev_ptr(out, torch.bfloat16, max(hi - lo, 0), "out")
+    _check(lib().zg_gather_params_mxfp8(ctx.handle, cp, sp, lo, hi, o, _stream(stream)), "zg_gather_params_mxfp8")
+
+
 def zg_quant_mxfp8(x: torch.Tensor, codes: torch.Tensor, scales: torch.Tensor, n: int | None = None,
                    stream=None) -> None:
     n = x.numel() if n is None else n
@@ -350,3 +384,15 @@ class ShardedAdamW:
 
     def info(self, stream=None) -> StepInfo:
         return zg_get_info(self.ctx, stream)
+
+    def gather(self, lo: int, hi: int, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+        """Stage three: parameters [lo, hi) gathered from the P rank shards of
+        the parameter vector (from the MX shards, decoded, when MX parameters
+        are bound) into ``out`` (allocated when None)."""
+        if out is None:
+            out = torch.empty(max(hi - lo, 0), dtype=torch.bfloat16, device=self.params.device)
+        if getattr(self, "pcodes", None) is not None:
+            zg_gather_params_mxfp8(self.ctx, self.pcodes, self.pscales, lo, hi, out, stream)
+        else:
+            zg_gather_params(self.ctx, self.params, lo, hi, out, stream)
+        return out

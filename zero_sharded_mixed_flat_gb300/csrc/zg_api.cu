@@ -417,6 +417,36 @@ int zg_set_wait_limit(zg_ctx *ctx, int64_t polls)
     return ZG_OK;
 }
 
+int zg_gather_params(const zg_ctx *ctx, const uint16_t *const *shards, int64_t lo, int64_t hi, uint16_t *out,
+                     zg_stream stream)
+{
+    if (int rc = check_ctx(ctx, false)) return rc;
+    if (lo < 0 || hi < lo || hi > ctx->n)
+        return fail(ZG_ERR_INVALID_ARG, "range [%lld, %lld) is not inside [0, N = %lld)", (long long)lo,
+                    (long long)hi, (long long)ctx->n);
+    if (lo == hi) return ZG_OK;
+    if (!out) return fail(ZG_ERR_INVALID_ARG, "out is NULL");
+    if (!aligned16(out)) return fail(ZG_ERR_MISALIGNED, "out must be 16-byte aligned");
+    if (int rc = check_rank_ptrs(ctx, shards, "shards", true)) return rc;
+    return finish_launch(zg::launch_gather(ctx->p, ctx->s, shards, lo, hi, out, stream), "parameter gather launch");
+}
+
+int zg_gather_params_mxfp8(const zg_ctx *ctx, const uint8_t *const *codes, const uint8_t *const *scales, int64_t lo,
+                           int64_t hi, uint16_t *out, zg_stream stream)
+{
+    if (int rc = check_ctx(ctx, false)) return rc;
+    if (lo < 0 || hi < lo || hi > ctx->n)
+        return fail(ZG_ERR_INVALID_ARG, "range [%lld, %lld) is not inside [0, N = %lld)", (long long)lo,
+                    (long long)hi, (long long)ctx->n);
+    if (lo == hi) return ZG_OK;
+    if (!out) return fail(ZG_ERR_INVALID_ARG, "out is NULL");
+    if (!aligned16(out)) return fail(ZG_ERR_MISALIGNED, "out must be 16-byte aligned");
+    if (int rc = check_rank_ptrs(ctx, codes, "codes", true)) return rc;
+    if (int rc = check_rank_ptrs(ctx, scales, "scales", false)) return rc;
+    return finish_launch(zg::launch_gather_mx(ctx->p, ctx->s, codes, scales, lo, hi, out, stream),
+                         "MX parameter gather launch");
+}
+
 int zg_probe_copy(const void *src, void *dst, int64_t bytes, zg_stream stream)
 {
     if (bytes < 0 || bytes % 16) return fail(ZG_ERR_INVALID_ARG, "bytes must be a non-negative multiple of 16");

@@ -27,6 +27,11 @@ cudaError_t launch_step_mx(int p, const uint8_t *const *c, const uint8_t *const 
                            StepK k, State state, Scalars *sc, cudaStream_t st);
 cudaError_t launch_quant(const uint16_t *in, int64_t n, uint8_t *codes, uint8_t *scales, cudaStream_t st);
 cudaError_t launch_copy(const void *src, void *dst, int64_t bytes, cudaStream_t st);
+// Stage three: gather parameters [lo, hi) from P shards of S elements each.
+cudaError_t launch_gather(int p, int64_t s, const uint16_t *const *shards, int64_t lo, int64_t hi, uint16_t *out,
+                          cudaStream_t st);
+cudaError_t launch_gather_mx(int p, int64_t s, const uint8_t *const *codes, const uint8_t *const *scales, int64_t lo,
+                             int64_t hi, uint16_t *out, cudaStream_t st);
 
 // Launch the step pass for one gradient source: grid = enough blocks for the
 // 8-element vectors, at most one wave; the MX-parameter instantiation when
