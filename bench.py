@@ -337,7 +337,8 @@ def time_stage3(opt, wl, K: int, peak: float, tokens: int = 8192) -> dict:
     (2 * tokens flops per parameter, cuBLAS). Serial: gather, then GEMM, layer
     by layer. Overlapped: layer i+1 is gathered on a second stream into the
     other of two buffers while layer i's GEMM runs (that stream at high or at
-    equal priority). Each sweep is captured once in a CUDA graph and replayed,
+    equal priority; for bf16 shards also with the copy-engine gather). Each
+    sweep is captured once in a CUDA graph and replayed,
     as a per-layer loop runs in production, so host launch costs stay out of
     the GPU times. Reported: per-sweep times and the gather time left exposed."""
     import torch
@@ -355,19 +356,21 @@ def time_stage3(opt, wl, K: int, peak: float, tokens: int = 8192) -> dict:
     gathered = [torch.cuda.Event() for _ in layers]
     used = [torch.cuda.Event(), torch.cuda.Event()]
 
-    def gather(i, b, st):
+    def gather(i, b, st, dma=False):
         lo, hi = layers[i]
-        opt.gather(lo, hi, bufs[b][:hi - lo], st)
+        opt.gather(lo, hi, bufs[b][:hi - lo], st, dma=dma)
 
     def compute(i, b):
         lo, hi = layers[i]
         k = (hi - lo) // d // 8 * 8  # an aligned leading dimension keeps cuBLAS on its tensor-core kernels
         torch.matmul(x, bufs[b][:k * d].view(d, k), out=y[:tokens * k].view(tokens, k))
 
-    def gathers_only():
-        cur = torch.cuda.current_stream()
-        for i in range(len(layers)):
-            gather(i, i % 2, cur)
+    def gathers_only(dma=False):
+        def run():
+            cur = torch.cuda.current_stream()
+            for i in range(len(layers)):
+                gather(i, i % 2, cur, dma)
+        return run
 
     def gemms_only():
         for i in range(len(layers)):
@@ -379,18 +382,18 @@ def time_stage3(opt, wl, K: int, peak: float, tokens: int = 8192) -> dict:
             gather(i, i % 2, cur)
             compute(i, i % 2)
 
-    def overlapped(side):
+    def overlapped(side, dma=False):
         def run():
             cur = torch.cuda.current_stream()
             side.wait_stream(cur)
-            gather(0, 0, side)
+            gather(0, 0, side, dma)
             gathered[0].record(side)
             for i in range(len(layers)):
                 b = i % 2
                 if i + 1 < len(layers):
                     if i >= 1:
                         side.wait_event(used[1 - b])  # layer i-1's GEMM is done with that buffer
-                    gather(i + 1, 1 - b, side)
+                    gather(i + 1, 1 - b, side, dma)
                     gathered[i + 1].record(side)
                 cur.wait_event(gathered[i])
                 compute(i, b)
@@ -415,7 +418,7 @@ def time_stage3(opt, wl, K: int, peak: float, tokens: int = 8192) -> dict:
         return e0.elapsed_time(e1) / K
 
     mx = getattr(opt, "pcodes", None) is not None
-    t_gather = timed(gathers_only)
+    t_gather = timed(gathers_only())
     t_gemm = timed(gemms_only)
     t_serial = timed(serial)
     t_hi = timed(overlapped(side_hi))
@@ -423,6 +426,12 @@ def time_stage3(opt, wl, K: int, peak: float, tokens: int = 8192) -> dict:
     per_param = accounting.mx_gather_bytes_per_param() if mx else accounting.gather_bytes_per_param()
     gbs = per_param * wl.n / (t_gather / 1e3) / 1e9
     flops = 2 * tokens * sum((hi - lo) // d // 8 * 8 * d for lo, hi in layers)
+    dma = {}
+    if not mx:  # the copy-engine gather (bf16 shards only)
+        t_dma = timed(gathers_only(True))
+        t_dma_ov = timed(overlapped(side_eq, True))
+        dma = {"gather_dma_ms": t_dma, "gather_dma_gbs": per_param * wl.n / (t_dma / 1e3) / 1e9,
+               "overlapped_dma_ms": t_dma_ov, "gather_exposed_overlapped_dma_ms": t_dma_ov - t_gemm}
     return {"layers": len(layers), "largest_layer": big, "shards": "MXFP8 codes + scales" if mx else "bf16",
             "timing": "each sweep captured in a CUDA graph, replayed",
             "gather_ms": t_gather, "gather_gbs": gbs, "gather_frac": gbs / peak,
@@ -432,6 +441,7 @@ def time_stage3(opt, wl, K: int, peak: float, tokens: int = 8192) -> dict:
             "serial_ms": t_serial, "overlapped_ms": t_hi, "overlapped_equal_priority_ms": t_eq,
             "gather_exposed_serial_ms": t_serial - t_gemm, "gather_exposed_overlapped_ms": t_hi - t_gemm,
             "gather_exposed_overlapped_equal_priority_ms": t_eq - t_gemm,
+            **dma,
             "ring_bytes_per_rank_per_sweep": accounting.ring_bytes_sent_per_rank(
                 (accounting.MX_BYTES_PER_ELEMENT if mx else accounting.PARAM_BF16) * wl.n, wl.p, "all_gather")}
 

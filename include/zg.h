@@ -240,6 +240,14 @@ int zg_set_wait_limit(zg_ctx *ctx, int64_t polls);
 int zg_gather_params(const zg_ctx *ctx, const uint16_t *const *shards, int64_t lo, int64_t hi, uint16_t *out,
                      zg_stream stream);
 
+/* zg_gather_params carried out by the copy engines instead of a kernel: one
+ * device-to-device cudaMemcpyAsync per shard the range crosses (at most P),
+ * enqueued on `stream`. Same arguments, result and errors; it occupies no
+ * SM, so it can run beside a computation that fills every SM (the layer
+ * before), which a gather kernel cannot. */
+int zg_gather_params_dma(const zg_ctx *ctx, const uint16_t *const *shards, int64_t lo, int64_t hi, uint16_t *out,
+                         zg_stream stream);
+
 /* The same gather from parameter shards stored as MXFP8 (Zero From Scratch,
  * item 14: MXFP8 on stored state, the layout zg_bind_params_mxfp8 writes):
  * codes[r] holds S E4M3 codes of rank r (16-byte aligned) and scales[r] its

@@ -58,6 +58,7 @@ def test_host_side_validation_needs_no_gpu(lib):
     assert b"multiple of 16" in lib.zg_last_error()
     assert lib.zg_gather_params(None, None, 0, 0, None, None) == zb.ZG_ERR_INVALID_ARG
     assert lib.zg_gather_params_mxfp8(None, None, None, 0, 0, None, None) == zb.ZG_ERR_INVALID_ARG
+    assert lib.zg_gather_params_dma(None, None, 0, 0, None, None) == zb.ZG_ERR_INVALID_ARG
     lib.zg_destroy(None)
 
 

@@ -52,8 +52,10 @@ def bf16_shards(n: int, p: int, seed: int):
     return s, host, dev
 
 
+@pytest.mark.parametrize("how", ["kernel", "dma"])
 @pytest.mark.parametrize("n,p", SIZES)
-def test_gather_bf16_matches_oracle(n, p):
+def test_gather_bf16_matches_oracle(n, p, how):
+    fn = zb.zg_gather_params if how == "kernel" else zb.zg_gather_params_dma
     ctx = zb.zg_init(n, p)
     s, host, dev = bf16_shards(n, p, seed=n + 7 * p)
     assert s == zb.zg_shard_len(ctx)
@@ -61,14 +63,14 @@ def test_gather_bf16_matches_oracle(n, p):
     checked = 0
     for lo, hi in ranges(n, s, seed=n):
         out.view.fill_(-1.0)
-        zb.zg_gather_params(ctx, [d.view for d in dev], lo, hi, out.view[:hi - lo])
+        fn(ctx, [d.view for d in dev], lo, hi, out.view[:hi - lo])
         got = to_host_u16(out.view)
         want = oracle.gather(host, s, lo, hi)
         assert np.array_equal(got[:hi - lo], want), (n, p, lo, hi, np.nonzero(got[:hi - lo] != want)[0][:5])
         assert np.all(got[hi - lo:] == 0xBF80), (n, p, lo, hi)  # -1.0 left alone past the range
         assert out.intact() and all(d.intact() for d in dev), (n, p, lo, hi)
         checked += 1
-    log({"case": f"gather bf16 n={n} p={p}", "ranges": checked, "bitexact": 1.0})
+    log({"case": f"gather bf16 ({how}) n={n} p={p}", "ranges": checked, "bitexact": 1.0})
 
 
 @pytest.mark.parametrize("n,p", SIZES)
@@ -195,6 +197,10 @@ def test_gather_argument_errors():
     null = zb._ptr_array([params.data_ptr() if r != 1 else 0 for r in range(p)])
     assert L.zg_gather_params(ctx.handle, null, 0, 16, out.data_ptr(), None) == zb.ZG_ERR_INVALID_ARG
     assert L.zg_gather_params(ctx.handle, None, 0, 16, out.data_ptr(), None) == zb.ZG_ERR_INVALID_ARG
+    assert L.zg_gather_params_dma(ctx.handle, ptrs, 0, n + 1, out.data_ptr(), None) == zb.ZG_ERR_INVALID_ARG
+    assert L.zg_gather_params_dma(ctx.handle, ptrs, 0, 16, out.data_ptr() + 2, None) == zb.ZG_ERR_MISALIGNED
+    assert L.zg_gather_params_dma(ctx.handle, null, 0, 16, out.data_ptr(), None) == zb.ZG_ERR_INVALID_ARG
+    assert L.zg_gather_params_dma(ctx.handle, ptrs, 7, 7, None, None) == zb.ZG_OK
     codes = torch.zeros(p * s, dtype=torch.uint8, device="cuda")
     scales = torch.zeros(p * s // 32, dtype=torch.uint8, device="cuda")
     cp = zb._ptr_array([codes.data_ptr() + r * s for r in range(p)])
@@ -222,6 +228,7 @@ def test_gather_in_cuda_graph():
     scales = torch.randint(110, 140, (p * s // 32,), dtype=torch.int32, device="cuda", generator=gen).to(torch.uint8)
     out = torch.zeros(n, dtype=torch.bfloat16, device="cuda")
     out_mx = torch.zeros(n, dtype=torch.bfloat16, device="cuda")
+    out_dma = torch.zeros(n, dtype=torch.bfloat16, device="cuda")
     zb.zg_gather_params(ctx, params, 0, 16, out[:16])  # launch configurations cached before capture
     zb.zg_gather_params_mxfp8(ctx, codes, scales, 0, 16, out_mx[:16])
     torch.cuda.synchronize()
@@ -230,6 +237,7 @@ def test_gather_in_cuda_graph():
         zb.zg_gather_params(ctx, params, 0, 100_000, out[:100_000])
         zb.zg_gather_params(ctx, params, 100_000, n, out[100_000:])
         zb.zg_gather_params_mxfp8(ctx, codes, scales, 0, n, out_mx)
+        zb.zg_gather_params_dma(ctx, params, 3, n, out_dma[:n - 3])
     hc, hs = codes.cpu().numpy(), scales.cpu().numpy()
     for k in range(2):
         if k:
@@ -238,9 +246,11 @@ def test_gather_in_cuda_graph():
             hc = codes.cpu().numpy()
         out.zero_()
         out_mx.zero_()
+        out_dma.zero_()
         g.replay()
         torch.cuda.synchronize()
         assert torch.equal(out.view(torch.int16), params[:n].view(torch.int16)), k
+        assert torch.equal(out_dma[:n - 3].view(torch.int16), params[3:n].view(torch.int16)), k
         want = oracle.gather_mx([hc[r * s:(r + 1) * s] for r in range(p)],
                                 [hs[r * s // 32:(r + 1) * s // 32] for r in range(p)], s, 0, n)
         assert np.array_equal(to_host_u16(out_mx), want), k

@@ -111,6 +111,7 @@ def lib() -> ctypes.CDLL:
             "zg_probe_copy": (ctypes.c_int, [_P, _P, _I64, _P]),
             "zg_gather_params": (ctypes.c_int, [_P, _P, _I64, _I64, _P, _P]),
             "zg_gather_params_mxfp8": (ctypes.c_int, [_P, _P, _P, _I64, _I64, _P, _P]),
+            "zg_gather_params_dma": (ctypes.c_int, [_P, _P, _I64, _I64, _P, _P]),
             "zg_grad_norm_noalloc": (ctypes.c_int, [_P, ctypes.c_int, _I64, ctypes.c_float, ctypes.c_int, _P, _P]),
             "zg_destroy": (None, [_P]),
             "zg_strerror": (ctypes.c_char_p, [ctypes.c_int]),
@@ -261,6 +262,13 @@ def zg_gather_params(ctx: Ctx, shards, lo: int, hi: int, out: torch.Tensor, stre
     _check(lib().zg_gather_params(ctx.handle, sp, lo, hi, o, _stream(stream)), "zg_gather_params")
 
 
+def zg_gather_params_dma(ctx: Ctx, shards, lo: int, hi: int, out: torch.Tensor, stream=None) -> None:
+    """zg_gather_params on the copy engines (one device-to-device copy per shard crossed)."""
+    sp = _shard_ptrs(ctx, shards, torch.bfloat16, 1, "shards")
+    o = _dev_ptr(out, torch.bfloat16, max(hi - lo, 0), "out")
+    _check(lib().zg_gather_params_dma(ctx.handle, sp, lo, hi, o, _stream(stream)), "zg_gather_params_dma")
+
+
 def zg_gather_params_mxfp8(ctx: Ctx, codes, scales, lo: int, hi: int, out: torch.Tensor, stream=None) -> None:
     """The gather from MXFP8 parameter shards, decoded to bf16. ``codes`` and
     ``scales``: P tensors each, or the whole code and scale vectors."""
@@ -385,14 +393,18 @@ class ShardedAdamW:
     def info(self, stream=None) -> StepInfo:
         return zg_get_info(self.ctx, stream)
 
-    def gather(self, lo: int, hi: int, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    def gather(self, lo: int, hi: int, out: torch.Tensor | None = None, stream=None,
+               dma: bool = False) -> torch.Tensor:
         """Stage three: parameters [lo, hi) gathered from the P rank shards of
         the parameter vector (from the MX shards, decoded, when MX parameters
-        are bound) into ``out`` (allocated when None)."""
+        are bound) into ``out`` (allocated when None); ``dma`` moves bf16
+        shards with the copy engines instead of a kernel."""
         if out is None:
             out = torch.empty(max(hi - lo, 0), dtype=torch.bfloat16, device=self.params.device)
         if getattr(self, "pcodes", None) is not None:
             zg_gather_params_mxfp8(self.ctx, self.pcodes, self.pscales, lo, hi, out, stream)
+        elif dma:
+            zg_gather_params_dma(self.ctx, self.params, lo, hi, out, stream)
         else:
             zg_gather_params(self.ctx, self.params, lo, hi, out, stream)
         return out

@@ -431,6 +431,29 @@ int zg_gather_params(const zg_ctx *ctx, const uint16_t *const *shards, int64_t l
     return finish_launch(zg::launch_gather(ctx->p, ctx->s, shards, lo, hi, out, stream), "parameter gather launch");
 }
 
+int zg_gather_params_dma(const zg_ctx *ctx, const uint16_t *const *shards, int64_t lo, int64_t hi, uint16_t *out,
+                         zg_stream stream)
+{
+    if (int rc = check_ctx(ctx, false)) return rc;
+    if (lo < 0 || hi < lo || hi > ctx->n)
+        return fail(ZG_ERR_INVALID_ARG, "range [%lld, %lld) is not inside [0, N = %lld)", (long long)lo,
+                    (long long)hi, (long long)ctx->n);
+    if (lo == hi) return ZG_OK;
+    if (!out) return fail(ZG_ERR_INVALID_ARG, "out is NULL");
+    if (!aligned16(out)) return fail(ZG_ERR_MISALIGNED, "out must be 16-byte aligned");
+    if (int rc = check_rank_ptrs(ctx, shards, "shards", true)) return rc;
+    // one device-to-device copy per shard the range crosses (at most P)
+    for (int64_t i = lo; i < hi;) {
+        const int64_t r = i / ctx->s;
+        const int64_t end = (r + 1) * ctx->s < hi ? (r + 1) * ctx->s : hi;
+        const cudaError_t e = cudaMemcpyAsync(out + (i - lo), shards[r] + (i - r * ctx->s),
+                                              size_t(end - i) * sizeof(uint16_t), cudaMemcpyDeviceToDevice, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "parameter gather copy");
+        i = end;
+    }
+    return ZG_OK;
+}
+
 int zg_gather_params_mxfp8(const zg_ctx *ctx, const uint8_t *const *codes, const uint8_t *const *scales, int64_t lo,
                            int64_t hi, uint16_t *out, zg_stream stream)
 {
