@@ -96,3 +96,42 @@ def test_mx_step_small(n, p):
         dec = ref.step_mx([c for c, _ in enc], [s for _, s in enc], 1.0)
         check_step(f"mx-step n={n} p={p}", run, ref, dec, info, k + 1)
     assert ref.t == 3
+
+
+def test_mx_step_raw_bytes():
+    """MX inputs as raw bytes rather than encoder output: random codes at
+    scales from subnormal (0) to large, blocks whose scale bytes (247..254)
+    the encoder never writes, a block whose products overflow and a NaN
+    code. Both ways the GPU sums decoded products (fused packed multiply-add
+    for ordinary scales, separate multiply and add otherwise) must match the
+    oracle, skips included."""
+    n, p = 65_549, 4
+    nb = (n + 31) // 32
+    rng = np.random.default_rng(77)
+    w0 = (rng.standard_normal(n) * 0.02).astype(np.float32)
+    run = GpuRun(w0, p)
+    ref = oracle.OracleOptimizer(w0)
+    big_blocks = rng.choice(nb, 40, replace=False)
+    for k in range(5):
+        codes, scales = [], []
+        for r in range(p):
+            c = rng.integers(0, 256, n).astype(np.uint8)
+            c[(c & 0x7F) == 0x7F] = 0x3A  # no NaN codes
+            s = rng.integers(100, 136, nb).astype(np.uint8)
+            s[rng.choice(nb, 30, replace=False)] = 0  # subnormal scale
+            s[big_blocks] = rng.integers(247, 255, big_blocks.size)
+            for b in big_blocks:  # those blocks hold zeros (finite products) ...
+                c[32 * b:32 * b + 32] = 0
+            codes.append(c)
+            scales.append(s)
+        if k == 2:  # ... except here: a product that overflows -> inf -> skip
+            codes[1][32 * int(big_blocks[0]) + 5] = 0x40
+        if k == 3:  # a NaN code -> skip
+            codes[2][n // 2] = 0xFF
+        zb.zg_step_mxfp8(run.ctx, [torch.from_numpy(c).cuda() for c in codes],
+                         [torch.from_numpy(s).cuda() for s in scales], 1.0)
+        info = zb.zg_get_info(run.ctx)
+        dec = ref.step_mx(codes, scales, 1.0)
+        assert bool(dec.found_inf) == (k in (2, 3)), (k, dec.found_inf)
+        check_step(f"mx-raw step {k + 1}", run, ref, dec, info, k + 1)
+    assert ref.t == 3

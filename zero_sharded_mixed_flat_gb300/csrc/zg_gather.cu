@@ -67,17 +67,6 @@ __device__ __forceinline__ uint32_t mx_to_bf16(float x)
     return x != x ? 0x7fc0u : uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(x)));
 }
 
-// Two binary32 products in one packed instruction, each rounded to nearest
-// even exactly as a scalar multiplication would be.
-__device__ __forceinline__ float2 mul_f32x2(float2 a, float2 b)
-{
-    uint64_t d;
-    asm("mul.rn.f32x2 %0, %1, %2;"
-        : "=l"(d)
-        : "l"(*reinterpret_cast<const uint64_t *>(&a)), "l"(*reinterpret_cast<const uint64_t *>(&b)));
-    return *reinterpret_cast<const float2 *>(&d);
-}
-
 // 16 codes of one block at one scale byte to 16 bf16 values (8 words, element
 // 2k in the low half). A NaN scale or any NaN code (0x7F / 0xFF, which the
 // encoder writes only into blocks with a NaN scale) sends the vector down the

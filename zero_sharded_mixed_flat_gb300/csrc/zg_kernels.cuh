@@ -153,6 +153,27 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
+// Two binary32 operations per instruction (Blackwell's packed fp32 pipe),
+// each lane rounded to nearest even exactly as its scalar form would be.
+__device__ __forceinline__ float2 mul_f32x2(float2 a, float2 b)
+{
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;"
+        : "=l"(d)
+        : "l"(*reinterpret_cast<const uint64_t *>(&a)), "l"(*reinterpret_cast<const uint64_t *>(&b)));
+    return *reinterpret_cast<const float2 *>(&d);
+}
+
+__device__ __forceinline__ float2 fma_f32x2(float2 a, float2 b, float2 c)
+{
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;"
+        : "=l"(d)
+        : "l"(*reinterpret_cast<const uint64_t *>(&a)), "l"(*reinterpret_cast<const uint64_t *>(&b)),
+          "l"(*reinterpret_cast<const uint64_t *>(&c)));
+    return *reinterpret_cast<const float2 *>(&d);
+}
+
 // ------------------------------------------------------------------ MXFP8
 
 // E8M0 scale byte to its value 2^(s - 127) as a binary32; 0 gives the
@@ -286,8 +307,38 @@ struct MxSrc {
         reduce(raw, out);
     }
 
+    // Each decoded product E4M3 * 2^(s - 127) is exact in binary32 while
+    // s <= 246 (the largest scale byte the encoder writes for finite data),
+    // so one fused multiply-add per element yields exactly the bits of the
+    // separate multiply and add, and the packed form takes two elements per
+    // instruction. A vector with a scale byte in 247..254 (which the encoder
+    // never writes) keeps the separate operations, where a product that
+    // overflows must read as inf before it is added.
     __device__ __forceinline__ void reduce(const Raw &raw, float (&out)[kVec]) const
     {
+        uint32_t big = 0u;
+#pragma unroll
+        for (int r = 0; r < P; ++r) big |= uint32_t(raw.sc[r] - 247u < 8u);
+        if (!big) {
+            float2 acc[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) acc[q] = make_float2(0.0f, 0.0f);
+#pragma unroll
+            for (int r = 0; r < P; ++r) {
+                const float scale = e8m0_value(raw.sc[r]);
+                const float2 s2 = make_float2(scale, scale);
+                const uint32_t w2[2] = {raw.x[r].x, raw.x[r].y};
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    acc[q] = fma_f32x2(e4m3x2_to_f32x2(uint16_t(w2[q >> 1] >> (16 * (q & 1)))), s2, acc[q]);
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                out[2 * q] = acc[q].x;
+                out[2 * q + 1] = acc[q].y;
+            }
+            return;
+        }
 #pragma unroll
         for (int j = 0; j < kVec; ++j) out[j] = 0.0f;
 #pragma unroll

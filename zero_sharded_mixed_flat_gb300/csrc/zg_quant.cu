@@ -6,59 +6,63 @@ namespace zg {
 // ------------------------------------------------------------------ MXFP8 encoder
 
 constexpr int kQuantThreads = 256;
+constexpr int kQuantVec = 16;  // elements per thread: two 16-byte bf16 loads, one 16-byte code store
 
-// Four lanes share one 32-element block (8 elements each): the block amax is
-// a max over the |x| bit patterns (non-negative bf16 order like integers),
-// combined across the four lanes with two xor shuffles. E8M0 byte from the
-// amax exponent field E: e = max(E - 135, -127), byte = e + 127.
+// Two lanes share one 32-element block (16 elements each). The block amax is
+// a max over the |x| bit patterns (non-negative bf16 order like unsigned
+// integers), taken on 16-bit pairs and combined across the two lanes with one
+// xor shuffle. E8M0 byte from the amax exponent field E: e = max(E - 135,
+// -127), byte = e + 127. x * 2^-e is exact wherever the E4M3 rounding can see
+// it, so the packed multiply gives the codes of the scalar one.
 __global__ void __launch_bounds__(kQuantThreads)
     quant_kernel(const uint16_t *__restrict__ in, int64_t n, uint8_t *__restrict__ codes,
                  uint8_t *__restrict__ scales)
 {
-    const int64_t nvec_full = n / kVec;
-    const int64_t nvec_all = (n + kVec - 1) / kVec;
+    const int64_t nvec_full = n / kQuantVec;
+    const int64_t nvec_all = (n + kQuantVec - 1) / kQuantVec;
     const int lane = threadIdx.x & 31;
     const int64_t stride = int64_t(gridDim.x) * kQuantThreads;
 #pragma unroll 1
     for (int64_t base = int64_t(blockIdx.x) * kQuantThreads + (threadIdx.x & ~31); base < nvec_all;
          base += stride) {
         const int64_t v = base + lane;
-        uint32_t wd[4] = {0u, 0u, 0u, 0u};
+        uint32_t wd[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
         if (v < nvec_full) {
-            const uint4 x = ld_stream(reinterpret_cast<const uint4 *>(in) + v);
-            wd[0] = x.x;
-            wd[1] = x.y;
-            wd[2] = x.z;
-            wd[3] = x.w;
+            const uint4 a = ld_stream(reinterpret_cast<const uint4 *>(in) + 2 * v);
+            const uint4 b = ld_stream(reinterpret_cast<const uint4 *>(in) + 2 * v + 1);
+            wd[0] = a.x, wd[1] = a.y, wd[2] = a.z, wd[3] = a.w;
+            wd[4] = b.x, wd[5] = b.y, wd[6] = b.z, wd[7] = b.w;
         } else if (v < nvec_all) {
 #pragma unroll
-            for (int j = 0; j < kVec; ++j)
-                if (v * kVec + j < n) wd[j >> 1] |= uint32_t(in[v * kVec + j]) << (16 * (j & 1));
+            for (int j = 0; j < kQuantVec; ++j)
+                if (v * kQuantVec + j < n) wd[j >> 1] |= uint32_t(in[v * kQuantVec + j]) << (16 * (j & 1));
         }
-        uint32_t amax = 0u;
+        uint32_t m2 = 0u;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) amax = max(amax, max(wd[q] & 0x7fffu, (wd[q] >> 16) & 0x7fffu));
+        for (int q = 0; q < 8; ++q) m2 = __vmaxu2(m2, wd[q] & 0x7fff7fffu);
+        uint32_t amax = max(m2 & 0xffffu, m2 >> 16);
         amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-        amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
         const bool bad = amax >= 0x7f80u;
         const uint32_t ex = amax >> 7;
         const uint32_t sbyte = bad ? 0xffu : (ex > 8u ? ex - 8u : 0u);
         const float to_unit = __uint_as_float((254u - (bad ? 0u : sbyte)) << 23);  // 2^-e
-        uint32_t pairs[4];
+        const float2 u2 = make_float2(to_unit, to_unit);
+        uint32_t pairs[8];
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
-            pairs[q] = bad ? 0x7f7fu
-                           : f32x2_to_e4m3x2(__fmul_rn(bf16_lo(wd[q]), to_unit),
-                                             __fmul_rn(bf16_hi(wd[q]), to_unit));
+        for (int q = 0; q < 8; ++q) {
+            const float2 y = mul_f32x2(make_float2(bf16_lo(wd[q]), bf16_hi(wd[q])), u2);
+            pairs[q] = bad ? 0x7f7fu : f32x2_to_e4m3x2(y.x, y.y);
+        }
         if (v < nvec_full) {
-            __stcs(reinterpret_cast<uint2 *>(codes) + v,
-                   make_uint2(pairs[0] | (pairs[1] << 16), pairs[2] | (pairs[3] << 16)));
+            __stcs(reinterpret_cast<uint4 *>(codes) + v,
+                   make_uint4(pairs[0] | (pairs[1] << 16), pairs[2] | (pairs[3] << 16), pairs[4] | (pairs[5] << 16),
+                              pairs[6] | (pairs[7] << 16)));
         } else if (v < nvec_all) {
 #pragma unroll
-            for (int j = 0; j < kVec; ++j)
-                if (v * kVec + j < n) codes[v * kVec + j] = uint8_t(pairs[j >> 1] >> (8 * (j & 1)));
+            for (int j = 0; j < kQuantVec; ++j)
+                if (v * kQuantVec + j < n) codes[v * kQuantVec + j] = uint8_t(pairs[j >> 1] >> (8 * (j & 1)));
         }
-        if ((lane & 3) == 0 && v < nvec_all) scales[v >> 2] = uint8_t(sbyte);
+        if ((lane & 1) == 0 && v < nvec_all) scales[v >> 1] = uint8_t(sbyte);
     }
 }
 
@@ -78,7 +82,7 @@ cudaError_t launch_quant(const uint16_t *in, int64_t n, uint8_t *codes, uint8_t 
 {
     if (n == 0) return cudaSuccess;
     const void *fn = reinterpret_cast<const void *>(&quant_kernel);
-    const int64_t nvec = (n + kVec - 1) / kVec;
+    const int64_t nvec = (n + kQuantVec - 1) / kQuantVec;
     const int64_t want = (nvec + kQuantThreads - 1) / kQuantThreads;
     const int wave = wave_blocks(fn, kQuantThreads, 0);
     const int blocks = int(want < wave ? want : wave);
