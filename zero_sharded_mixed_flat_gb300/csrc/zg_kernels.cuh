@@ -504,6 +504,40 @@ __device__ __forceinline__ void finalize_decision(Scalars *sc, double sumsq, con
     sc->norm_gen = sc->norm_gen + 1u;
 }
 
+// The end of every norm pass: the block's fixed-tree sum of the threads'
+// fp64 partials goes to partials[blockIdx.x]; the last block to finish (an
+// atomic ticket) sums the block partials in index order and writes the
+// decision (or, for a bucket, adds to the running bucket sum).
+__device__ __forceinline__ void norm_finish(double acc, double *__restrict__ partials, Scalars *sc,
+                                            const FinalizeK &fk, int mode)
+{
+    __shared__ double red[kNormThreads / 32];
+    __shared__ int am_last;
+    const double bsum = block_sum<kNormThreads>(acc, red);
+    if (threadIdx.x == 0) {
+        partials[blockIdx.x] = bsum;
+        __threadfence();
+        const unsigned int ticket = atomicAdd(&sc->norm_ticket, 1u);
+        am_last = (ticket == gridDim.x - 1);
+    }
+    __syncthreads();
+    if (!am_last) return;
+    __threadfence();
+    double s = 0.0;
+    for (int i = threadIdx.x; i < int(gridDim.x); i += kNormThreads) s += __ldcg(partials + i);
+    const double total = block_sum<kNormThreads>(s, red);
+    if (threadIdx.x == 0) {
+        if (!(mode & kNormBucket)) {
+            finalize_decision(sc, total, fk);
+        } else {
+            const double run = (mode & kNormFirst) ? total : sc->bucket_acc + total;
+            sc->bucket_acc = run;
+            if (mode & kNormLast) finalize_decision(sc, run, fk);
+        }
+        sc->norm_ticket = 0u;
+    }
+}
+
 // Grid-stride over 8-element vectors. Each thread owns a fixed set of
 // vectors (a function of N and the grid only), squares g in fp32, adds runs
 // of 32 squares with two-sum and widens each run to fp64; blocks reduce in a
@@ -514,8 +548,6 @@ __global__ void __launch_bounds__(kNormThreads, NormMinBlocks<Src>::value)
     norm_kernel(Src src, int64_t n, float inv, double *__restrict__ partials, Scalars *sc, FinalizeK fk,
                 float *__restrict__ stage = nullptr, int mode = kNormWhole)
 {
-    __shared__ double red[kNormThreads / 32];
-    __shared__ int am_last;
     pdl_wait();     // the gradients may come from the kernel just before
     pdl_trigger();  // the step pass may start its blocks as ours retire
     const int64_t nvec = n / kVec;
@@ -574,29 +606,7 @@ __global__ void __launch_bounds__(kNormThreads, NormMinBlocks<Src>::value)
             if (kStage) stage[i] = g;
         }
     }
-    const double bsum = block_sum<kNormThreads>(acc, red);
-    if (threadIdx.x == 0) {
-        partials[blockIdx.x] = bsum;
-        __threadfence();
-        const unsigned int ticket = atomicAdd(&sc->norm_ticket, 1u);
-        am_last = (ticket == gridDim.x - 1);
-    }
-    __syncthreads();
-    if (!am_last) return;
-    __threadfence();
-    double s = 0.0;
-    for (int i = threadIdx.x; i < int(gridDim.x); i += kNormThreads) s += __ldcg(partials + i);
-    const double total = block_sum<kNormThreads>(s, red);
-    if (threadIdx.x == 0) {
-        if (!(mode & kNormBucket)) {
-            finalize_decision(sc, total, fk);
-        } else {
-            const double acc = (mode & kNormFirst) ? total : sc->bucket_acc + total;
-            sc->bucket_acc = acc;
-            if (mode & kNormLast) finalize_decision(sc, acc, fk);
-        }
-        sc->norm_ticket = 0u;
-    }
+    norm_finish(acc, partials, sc, fk, mode);
 }
 
 // ------------------------------------------------------------------ fused step pass
