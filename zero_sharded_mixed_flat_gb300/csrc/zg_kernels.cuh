@@ -963,8 +963,11 @@ cudaError_t with_ranks(int p, F &&f)
 namespace zg {
 namespace tma {
 
-constexpr int kTile = 2048;          // elements per tile: 8 per thread at 256 threads
-constexpr int kThreads = 256;
+#ifndef ZG_TMA_TILE
+#define ZG_TMA_TILE 2048
+#endif
+constexpr int kTile = ZG_TMA_TILE;    // elements per tile
+constexpr int kThreads = kTile / kVec;  // 8 elements per thread
 constexpr long long kDrainLimit = 1LL << 22;
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p)

@@ -7,6 +7,10 @@ namespace zg {
 #define ZG_TMA_CTAS_PER_SM 2
 #endif
 constexpr int kTmaCtasPerSm = ZG_TMA_CTAS_PER_SM;
+#ifndef ZG_TMA_MAX_STAGES
+#define ZG_TMA_MAX_STAGES 4
+#endif
+static_assert(ZG_TMA_MAX_STAGES >= 2 && ZG_TMA_MAX_STAGES <= 8, "the kernel holds eight barriers");
 
 cudaError_t launch_step_tma(int p, const uint16_t *const *g, int64_t n, float inv, StepK k, State state, Scalars *sc,
                             long long wait_limit, cudaStream_t st)
@@ -16,13 +20,13 @@ cudaError_t launch_step_tma(int p, const uint16_t *const *g, int64_t n, float in
         Bf16Src<P> src;
         for (int r = 0; r < P; ++r) src.g[r] = g[r];
         const tma::Layout lay = tma::Layout::of(P);
-        // Ring buffers per CTA: as many (2..4) as fit when kTmaCtasPerSm CTAs
+        // Ring buffers per CTA: as many (2..ZG_TMA_MAX_STAGES) as fit when kTmaCtasPerSm CTAs
         // share an SM's 228 KB, so that more warps hide each tile's compute;
         // if two buffers do not fit that way (large P), one CTA per SM.
         const int sm_bytes = 227 * 1024 - 1024;
         int stages = sm_bytes / kTmaCtasPerSm / int(lay.stage_bytes);
         if (stages < 2) stages = sm_bytes / int(lay.stage_bytes);
-        stages = stages > 4 ? 4 : stages;
+        stages = stages > ZG_TMA_MAX_STAGES ? ZG_TMA_MAX_STAGES : stages;
         if (stages < 2) return cudaErrorInvalidConfiguration;
         const size_t smem = size_t(stages) * lay.stage_bytes;
         auto *fn = &tma::step_kernel_tma<P>;
