@@ -672,7 +672,11 @@ def bench_ours(args, rank: int, world: int, local: int) -> dict | None:
     value = world * n * K / t_max
 
     peak, peak_kind = measured_peaks()
-    if wl.mx:
+    if wl.mx and args.variant == "staged":
+        b_step = accounting.staged_shard_step_bytes_per_param() * n
+        b_norm = accounting.mx_staged_grad_norm_bytes_per_param(p) * n
+        b_quant = accounting.mx_quant_bytes_per_param() * p * n
+    elif wl.mx:
         b_step = accounting.mx_shard_step_bytes_per_param(p) * n
         b_norm = accounting.mx_grad_norm_bytes_per_param(p) * n
         b_quant = accounting.mx_quant_bytes_per_param() * p * n
@@ -744,8 +748,7 @@ def bench_ours(args, rank: int, world: int, local: int) -> dict | None:
     stage3 = time_stage3(opt, wl, max(3, min(K, 20)), peak) if args.stage3 else None
     graph = (time_graph(opt, dev, ls, K) if not wl.mx and args.variant == "ldg" and not args.offload
              and args.params == "bf16" and not args.no_alternatives and world == 1 else None)
-    step_kernel = ("zg_shard_step_mxfp8" if wl.mx else
-                   "zg_shard_step_staged" if args.variant == "staged" else "zg_shard_step")
+    step_kernel = ("zg_shard_step_mxfp8" if wl.mx else "zg_shard_step") + ("_staged" if args.variant == "staged" else "")
     if args.params == "mxfp8":
         step_kernel += "_mxparams"
     alternatives = {}

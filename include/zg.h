@@ -211,7 +211,9 @@ int zg_bind_grad_stage(zg_ctx *ctx, float *stage);
 
 /* Choose how bf16 steps run: ZG_VARIANT_LDG, ZG_VARIANT_TMA or
  * ZG_VARIANT_STAGED (which needs zg_bind_grad_stage first, else
- * ZG_ERR_NOT_BOUND). The MX path always runs the fused plain-load kernels. */
+ * ZG_ERR_NOT_BOUND). The MX path follows ZG_VARIANT_STAGED too (its norm pass
+ * stores the reduced gradient, its step pass reads it) and otherwise runs
+ * its fused plain-load kernels. */
 int zg_set_variant(zg_ctx *ctx, int variant);
 
 /* Bound, in polls, on each device-side wait of the TMA variant (default a

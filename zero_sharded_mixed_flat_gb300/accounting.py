@@ -137,6 +137,11 @@ def mx_grad_norm_bytes_per_param(p: int) -> float:
     return MX_BYTES_PER_ELEMENT * p
 
 
+def mx_staged_grad_norm_bytes_per_param(p: int) -> float:
+    """MX norm pass that also stores the reduced fp32 gradient."""
+    return MX_BYTES_PER_ELEMENT * p + 4
+
+
 def mx_shard_step_bytes_per_param(p: int) -> float:
     return MX_BYTES_PER_ELEMENT * p + 2 * OPTIMIZER_STATE + PARAM_BF16
 

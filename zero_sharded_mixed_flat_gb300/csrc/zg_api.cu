@@ -331,7 +331,8 @@ int zg_grad_norm_mxfp8(zg_ctx *ctx, const uint8_t *const *codes, const uint8_t *
     if (int rc = check_rank_ptrs(ctx, codes, "codes", true)) return rc;
     if (int rc = check_rank_ptrs(ctx, scales, "scales", false)) return rc;
     return finish_launch(zg::launch_norm_mx(ctx->p, codes, scales, ctx->n, inv_scale(ctx, loss_scale), ctx->d_partials,
-                                            ctx->partials_cap, ctx->d_sc, ctx->fk, stream),
+                                            ctx->partials_cap, ctx->d_sc, ctx->fk, stream,
+                                            ctx->variant == ZG_VARIANT_STAGED ? ctx->stage : nullptr),
                          "MX norm pass launch");
 }
 
@@ -342,6 +343,9 @@ int zg_shard_step_mxfp8(zg_ctx *ctx, const uint8_t *const *codes, const uint8_t 
     if (int rc = check_scale(loss_scale)) return rc;
     if (int rc = check_rank_ptrs(ctx, codes, "codes", true)) return rc;
     if (int rc = check_rank_ptrs(ctx, scales, "scales", false)) return rc;
+    if (ctx->variant == ZG_VARIANT_STAGED)
+        return finish_launch(zg::launch_step_staged(ctx->stage, ctx->n, ctx->k, state_of(ctx), ctx->d_sc, stream),
+                             "staged step pass launch");
     return finish_launch(zg::launch_step_mx(ctx->p, codes, scales, ctx->n, inv_scale(ctx, loss_scale), ctx->k,
                                             state_of(ctx), ctx->d_sc, stream),
                          "MX step pass launch");

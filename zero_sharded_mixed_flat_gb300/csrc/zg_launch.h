@@ -16,8 +16,10 @@ int wave_blocks(const void *kernel, int threads, size_t smem);
 cudaError_t launch_norm_bf16(int p, const uint16_t *const *g, int64_t n, float inv, double *partials,
                              int max_blocks, Scalars *sc, FinalizeK fk, cudaStream_t st, float *stage = nullptr,
                              int mode = kNormWhole);
+// With `stage` non-null the pass also writes the unscaled fp32 gradient there.
 cudaError_t launch_norm_mx(int p, const uint8_t *const *c, const uint8_t *const *s, int64_t n, float inv,
-                           double *partials, int max_blocks, Scalars *sc, FinalizeK fk, cudaStream_t st);
+                           double *partials, int max_blocks, Scalars *sc, FinalizeK fk, cudaStream_t st,
+                           float *stage = nullptr);
 cudaError_t launch_step_bf16(int p, const uint16_t *const *g, int64_t n, float inv, StepK k, State state,
                              Scalars *sc, cudaStream_t st);
 cudaError_t launch_step_staged(const float *stage, int64_t n, StepK k, State state, Scalars *sc, cudaStream_t st);

@@ -69,9 +69,12 @@ __device__ __forceinline__ void mx_reduce16(const uint4 (&c)[P], const uint32_t 
 // two-sum pair, each run widened to fp64. A run whose fp32 pair is not finite
 // is redone with every square widened on its own, so the result is non-finite
 // exactly when some square is. Same N, P and grid: bit-identical norm.
-template <int P>
+// With kStage the pass also stores the unscaled, averaged gradient g (the
+// reduce-scatter output) for the staged step pass.
+template <int P, bool kStage>
 __global__ void __launch_bounds__(kNormThreads, MxNormMinBlocks<P>::value)
-    norm_mx_kernel(MxSrc<P> src, int64_t n, float inv, double *__restrict__ partials, Scalars *sc, FinalizeK fk)
+    norm_mx_kernel(MxSrc<P> src, int64_t n, float inv, double *__restrict__ partials, Scalars *sc, FinalizeK fk,
+                   float *__restrict__ stage)
 {
     pdl_wait();
     pdl_trigger();
@@ -100,6 +103,13 @@ __global__ void __launch_bounds__(kNormThreads, MxNormMinBlocks<P>::value)
                 const float2 sq = mul_f32x2(gg, gg);
                 two_sum_acc(hi, lo, sq.x);
                 two_sum_acc(hi, lo, sq.y);
+                g[j] = gg.x;
+                g[j + 1] = gg.y;
+            }
+            if (kStage) {
+                float4 *o = reinterpret_cast<float4 *>(stage) + 4 * v;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) __stcs(o + q, make_float4(g[4 * q], g[4 * q + 1], g[4 * q + 2], g[4 * q + 3]));
             }
         }
         if (isfinite(hi) && isfinite(lo)) {
@@ -120,13 +130,14 @@ __global__ void __launch_bounds__(kNormThreads, MxNormMinBlocks<P>::value)
         for (int64_t i = nvec * kMxNormVec; i < n; ++i) {  // ragged tail, fewer than 16 elements
             const float g = __fmul_rn(src.sum1(i), inv);
             acc += double(__fmul_rn(g, g));
+            if (kStage) stage[i] = g;
         }
     }
     norm_finish(acc, partials, sc, fk, kNormWhole);
 }
 
 cudaError_t launch_norm_mx(int p, const uint8_t *const *c, const uint8_t *const *s, int64_t n, float inv,
-                           double *partials, int max_blocks, Scalars *sc, FinalizeK fk, cudaStream_t st)
+                           double *partials, int max_blocks, Scalars *sc, FinalizeK fk, cudaStream_t st, float *stage)
 {
     return with_ranks(p, [&](auto rk) {
         constexpr int P = decltype(rk)::value;
@@ -135,12 +146,12 @@ cudaError_t launch_norm_mx(int p, const uint8_t *const *c, const uint8_t *const 
             src.c[r] = c[r];
             src.s[r] = s[r];
         }
-        const void *fn = reinterpret_cast<const void *>(&norm_mx_kernel<P>);
+        auto *kernel = stage ? &norm_mx_kernel<P, true> : &norm_mx_kernel<P, false>;
         const int64_t want = (n / kMxNormVec + kNormThreads - 1) / kNormThreads;
         int blocks = int(want < 1 ? 1 : (want < max_blocks ? want : max_blocks));
-        const int wave = wave_blocks(fn, kNormThreads, 0);
+        const int wave = wave_blocks(reinterpret_cast<const void *>(kernel), kNormThreads, 0);
         if (blocks > wave) blocks = wave;
-        return launch_dependent(&norm_mx_kernel<P>, blocks, kNormThreads, 0, st, src, n, inv, partials, sc, fk);
+        return launch_dependent(kernel, blocks, kNormThreads, 0, st, src, n, inv, partials, sc, fk, stage);
     });
 }
 
