@@ -289,8 +289,6 @@ struct MxSrc {
         for (int r = 0; r < P; ++r) prefetch_l2(c[r] + vec * kVec);
     }
 
-    __device__ __forceinline__ void load_norm(int64_t vec, Raw &raw) const { load(vec, raw); }
-
     __device__ __forceinline__ void load(int64_t vec, Raw &raw) const
     {
 #pragma unroll
@@ -298,13 +296,6 @@ struct MxSrc {
             raw.x[r] = ld_stream(reinterpret_cast<const uint2 *>(c[r]) + vec);
             raw.sc[r] = s[r][vec >> 2];
         }
-    }
-
-    __device__ __forceinline__ void sum8(int64_t vec, float (&out)[kVec]) const
-    {
-        Raw raw;
-        load(vec, raw);
-        reduce(raw, out);
     }
 
     // Each decoded product E4M3 * 2^(s - 127) is exact in binary32 while
@@ -389,13 +380,6 @@ struct StagedSrc {
     {
         out[0] = raw.a.x, out[1] = raw.a.y, out[2] = raw.a.z, out[3] = raw.a.w;
         out[4] = raw.b.x, out[5] = raw.b.y, out[6] = raw.b.z, out[7] = raw.b.w;
-    }
-
-    __device__ __forceinline__ void sum8(int64_t vec, float (&out)[kVec]) const
-    {
-        Raw raw;
-        load(vec, raw);
-        reduce(raw, out);
     }
 
     __device__ __forceinline__ float sum1(int64_t i) const { return g[i]; }
