@@ -20,7 +20,8 @@ from zero_sharded_mixed_flat_gb300 import synth
 pytestmark = pytest.mark.gpu
 
 POISON_BF16 = 0x7FC1
-SIZES = [(1, 1), (31, 2), (1000, 3), (4099, 4), (65_549, 4), (65_536, 16), (200_003, 8), ((1 << 20) + 40, 8)]
+SIZES = [(1, 1), (31, 2), (1000, 3), (4099, 4), (65_549, 4), (30_001, 5), (77_777, 11), (65_536, 16), (200_003, 8),
+         ((1 << 20) + 40, 8)]
 
 
 def ranges(n: int, s: int, seed: int, extra: int = 40):

@@ -77,7 +77,7 @@ def test_quant_empty_and_tiny():
                       torch.zeros(1, dtype=torch.uint8, device="cuda"), n=0)
 
 
-@pytest.mark.parametrize("n,p", [(1, 1), (33, 2), (1000, 3), (65_549, 8), (4096, 16)])
+@pytest.mark.parametrize("n,p", [(1, 1), (33, 2), (1000, 3), (30_001, 5), (65_549, 8), (20_011, 11), (4096, 16)])
 def test_mx_step_small(n, p):
     rng = np.random.default_rng(n + p)
     w0 = (rng.standard_normal(n) * 0.02).astype(np.float32)
