@@ -748,7 +748,8 @@ def bench_ours(args, rank: int, world: int, local: int) -> dict | None:
     stage3 = time_stage3(opt, wl, max(3, min(K, 20)), peak) if args.stage3 else None
     graph = (time_graph(opt, dev, ls, K) if not wl.mx and args.variant == "ldg" and not args.offload
              and args.params == "bf16" and not args.no_alternatives and world == 1 else None)
-    step_kernel = ("zg_shard_step_mxfp8" if wl.mx else "zg_shard_step") + ("_staged" if args.variant == "staged" else "")
+    step_kernel = (("zg_shard_step_mxfp8" if wl.mx else "zg_shard_step")
+                   + {"staged": "_staged", "tma": "" if wl.mx else "_tma"}.get(args.variant, ""))
     if args.params == "mxfp8":
         step_kernel += "_mxparams"
     alternatives = {}
