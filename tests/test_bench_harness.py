@@ -48,7 +48,7 @@ def test_reference_arm_prints_the_contract_line():
                 "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
         assert key in line, key
     assert line["impl"] == "reference" and line["value"] > 0 and line["unit"] == "params/s"
-    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] == 1
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] == bench.host_threads()
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["value"] == line["value"]
     assert line["config"]["workload"] == "flat65k_p4"
 
@@ -78,3 +78,25 @@ def test_roofline_bookkeeping(monkeypatch, tmp_path):
     assert bench.recorded_traffic("zg_shard_step", "w") == 123.0
     assert bench.recorded_traffic("zg_shard_step", "old") is None  # counters from other sources
     assert bench.recorded_traffic("zg_shard_step", "missing") is None
+
+
+def test_threaded_oracle_matches_the_oracle():
+    """The bench's many-thread oracle timing runs the oracle's own range
+    functions; its state after a few steps equals the one-thread oracle's
+    (bit for bit while the clip is inactive, as on this workload)."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    import bench
+    import oracle
+    from zero_sharded_mixed_flat_gb300 import synth
+
+    wl = synth.workload("flat65k_p4")
+    ns = 65_536
+    with ThreadPoolExecutor(4) as ex:
+        _, w, m, v, t = bench.oracle_threaded_steps(wl, ns, 3, ex)
+    ref = oracle.OracleOptimizer(synth.init_weights(wl, 0, ns))
+    g = [synth.grads_bf16(wl, 1, r, 0, ns) for r in range(wl.p)]
+    for _ in range(3):
+        dec = ref.step(g, wl.loss_scale)
+    assert dec.clip == 1.0 and t == ref.t == 3
+    assert w.tobytes() == ref.w.tobytes() and m.tobytes() == ref.m.tobytes() and v.tobytes() == ref.v.tobytes()
