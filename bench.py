@@ -259,6 +259,8 @@ def oracle_threaded_steps(workload, ns: int, k: int, ex) -> tuple:
     w = synth.init_weights(workload, 0, ns).copy()
     m = np.zeros(ns, np.float32)
     v = np.zeros(ns, np.float32)
+    m.fill(0.0)  # touch the pages before the timed region
+    v.fill(0.0)
     grads = [synth.grads_bf16(workload, 1, r, 0, ns) for r in range(p)]
     cut = sorted({min(ns, ns * i // threads // 32 * 32) for i in range(threads)} | {ns})
     ranges = [(a, b) for a, b in zip(cut[:-1], cut[1:]) if b > a]
