@@ -831,9 +831,10 @@ __global__ void __launch_bounds__(kStepThreads, StepMinBlocks<Src>::value)
     // first vector (inputs the norm pass does not write), then wait for the
     // norm pass's decision before reading it.
     {
+        const int64_t nv = kMxOut ? (n / 32) * 4 : n / kVec;  // vectors the main loop walks
         int64_t v0 = int64_t(blockIdx.x) * kStepThreads + threadIdx.x;
-        if (ZG_STEP_REVERSE && !kMxOut) v0 = n / kVec - 1 - v0;
-        if (v0 >= 0 && v0 < n / kVec) {
+        if (ZG_STEP_REVERSE) v0 = nv - 1 - v0;
+        if (v0 >= 0 && v0 < nv) {
             src.prefetch(v0);
             prefetch_l2(st.w + v0 * kVec);
             prefetch_l2(st.m + v0 * kVec);
@@ -845,14 +846,17 @@ __global__ void __launch_bounds__(kStepThreads, StepMinBlocks<Src>::value)
     float c, bc1, bc2;
     const int skip = step_prologue(sc, c, bc1, bc2);
     if (skip == 0 && kMxOut) {
-        // whole 32-blocks: a warp-uniform loop so four lanes can share a block
+        // whole 32-blocks: a warp-uniform loop so four lanes can share a block.
+        // Walked from the end like the plain loop: mirroring the index keeps
+        // each four-lane group on one whole block (nvec and base are
+        // multiples of 4), only in reverse lane order.
         const int64_t nvec = (n / 32) * 4;
         const int64_t stride = int64_t(gridDim.x) * kStepThreads;
         const int lane = threadIdx.x & 31;
 #pragma unroll 1
         for (int64_t base = int64_t(blockIdx.x) * kStepThreads + (threadIdx.x & ~31); base < nvec; base += stride) {
-            const int64_t v = base + lane;
-            const bool active = v < nvec;
+            const bool active = base + lane < nvec;
+            const int64_t v = ZG_STEP_REVERSE ? nvec - 1 - (base + lane) : base + lane;
             float w[kVec] = {}, m[kVec], vv[kVec];
             if (active) {
                 VecData<Src> d;
