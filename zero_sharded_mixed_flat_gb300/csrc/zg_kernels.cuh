@@ -955,6 +955,9 @@ namespace tma {
 #define ZG_TMA_TILE 2048
 #endif
 constexpr int kTile = ZG_TMA_TILE;    // elements per tile
+#ifndef ZG_TMA_REVERSE
+#define ZG_TMA_REVERSE ZG_STEP_REVERSE
+#endif
 constexpr int kThreads = kTile / kVec;  // 8 elements per thread
 constexpr long long kDrainLimit = 1LL << 22;
 
@@ -1051,9 +1054,15 @@ __global__ void __launch_bounds__(kThreads)
     __syncthreads();
 
     auto stage_ptr = [&](int s) { return smem + size_t(s) * lay.stage_bytes; };
+    // first element of this CTA's j-th tile; the tiles are walked from the
+    // end, like the plain kernel's vectors, where the norm pass finished
+    auto tile_start = [&](int64_t j) {
+        const int64_t t = int64_t(blockIdx.x) + j * gridDim.x;
+        return (ZG_TMA_REVERSE ? ntiles - 1 - t : t) * kTile;
+    };
     auto issue = [&](int64_t j) {  // thread 0: start the copies of this CTA's j-th tile
         const int s = int(j % stages);
-        const int64_t t0 = (int64_t(blockIdx.x) + j * gridDim.x) * kTile;
+        const int64_t t0 = tile_start(j);
         const int64_t len = covered - t0 < kTile ? covered - t0 : kTile;
         unsigned char *buf = stage_ptr(s);
         const uint32_t gb = uint32_t(len * 2), fb = uint32_t(len * 4);
@@ -1079,7 +1088,7 @@ __global__ void __launch_bounds__(kThreads)
         if (timed_out) atomicExch(&s_timeout, 1);
         __syncthreads();
         if (s_timeout) break;
-        const int64_t t0 = (int64_t(blockIdx.x) + j * gridDim.x) * kTile;
+        const int64_t t0 = tile_start(j);
         const int64_t len = covered - t0 < kTile ? covered - t0 : kTile;
         const int e = threadIdx.x * kVec;
         if (e < len) {
