@@ -239,10 +239,11 @@ def time_oracle(workload, budget_s: float, steps: int, warmup: int = 0) -> dict:
             "seconds": el}
 
 
-def oracle_threaded_steps(workload, ns: int, k: int, ex) -> tuple:
+def oracle_threaded_steps(workload, ns: int, k: int, ex, threads: int) -> tuple:
     """``k`` oracle steps on the first ``ns`` parameters of the workload, the
-    work spread over the executor ``ex`` as contiguous index ranges cut at
-    multiples of 32 (the oracle's C calls release the interpreter lock):
+    work spread over the executor ``ex`` (``threads`` workers) as contiguous
+    index ranges cut at multiples of 32 (the oracle's C calls release the
+    interpreter lock):
     reduce-scatter and sum of squares per range (on the MX workload each
     rank's encode per range first), the fp64 partials added in range order,
     one decision, AdamW per range. Same arithmetic as the one-thread oracle;
@@ -255,7 +256,6 @@ def oracle_threaded_steps(workload, ns: int, k: int, ex) -> tuple:
 
     hp = oracle.Hparams()
     p = workload.p
-    threads = ex._max_workers
     w = synth.init_weights(workload, 0, ns).copy()
     m = np.zeros(ns, np.float32)
     v = np.zeros(ns, np.float32)
@@ -300,12 +300,12 @@ def time_oracle_threads(workload, budget_s: float, steps: int, threads: int, war
 
     with ThreadPoolExecutor(threads) as ex:
         probe = min(workload.n, 1 << 20)
-        rate = probe / max(oracle_threaded_steps(workload, probe, 2, ex)[0] / 2, 1e-9)
+        rate = probe / max(oracle_threaded_steps(workload, probe, 2, ex, threads)[0] / 2, 1e-9)
         ns = int(min(workload.n, max(1 << 16, rate * budget_s)))
         ns = max(32, ns // 32 * 32)
         if warmup:
-            oracle_threaded_steps(workload, ns, warmup, ex)
-        el = oracle_threaded_steps(workload, ns, steps, ex)[0]
+            oracle_threaded_steps(workload, ns, warmup, ex, threads)
+        el = oracle_threaded_steps(workload, ns, steps, ex, threads)[0]
     return {"value": ns * steps / el, "unit": UNIT, "cores": threads, "kind": "oracle",
             "sample": f"first {ns} of {workload.n} params, all {workload.p} ranks, {steps} steps, "
                       f"{threads} threads on contiguous ranges", "seconds": el}

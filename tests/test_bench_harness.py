@@ -93,7 +93,7 @@ def test_threaded_oracle_matches_the_oracle():
     wl = synth.workload("flat65k_p4")
     ns = 65_536
     with ThreadPoolExecutor(4) as ex:
-        _, w, m, v, t = bench.oracle_threaded_steps(wl, ns, 3, ex)
+        _, w, m, v, t = bench.oracle_threaded_steps(wl, ns, 3, ex, 4)
     ref = oracle.OracleOptimizer(synth.init_weights(wl, 0, ns))
     g = [synth.grads_bf16(wl, 1, r, 0, ns) for r in range(wl.p)]
     for _ in range(3):
