@@ -98,6 +98,23 @@ zg::State state_of(const zg_ctx *ctx)
     return zg::State{ctx->w, ctx->m, ctx->v, ctx->params, ctx->pcodes, ctx->pscales};
 }
 
+// Checks shared by the gathers: a context, a range inside [0, N) and a
+// 16-byte aligned output. Returns a ZG_ERR_* code, ZG_OK to go on, or
+// kNothingToDo for an empty range (which needs no pointers at all).
+constexpr int kNothingToDo = 1;
+
+int check_gather(const zg_ctx *ctx, int64_t lo, int64_t hi, const void *out)
+{
+    if (int rc = check_ctx(ctx, false)) return rc;
+    if (lo < 0 || hi < lo || hi > ctx->n)
+        return fail(ZG_ERR_INVALID_ARG, "range [%lld, %lld) is not inside [0, N = %lld)", (long long)lo,
+                    (long long)hi, (long long)ctx->n);
+    if (lo == hi) return kNothingToDo;
+    if (!out) return fail(ZG_ERR_INVALID_ARG, "out is NULL");
+    if (!aligned16(out)) return fail(ZG_ERR_MISALIGNED, "out must be 16-byte aligned");
+    return ZG_OK;
+}
+
 int finish_launch(cudaError_t e, const char *what) { return e == cudaSuccess ? ZG_OK : cuda_fail(e, what); }
 
 }  // namespace
@@ -424,13 +441,7 @@ int zg_set_wait_limit(zg_ctx *ctx, int64_t polls)
 int zg_gather_params(const zg_ctx *ctx, const uint16_t *const *shards, int64_t lo, int64_t hi, uint16_t *out,
                      zg_stream stream)
 {
-    if (int rc = check_ctx(ctx, false)) return rc;
-    if (lo < 0 || hi < lo || hi > ctx->n)
-        return fail(ZG_ERR_INVALID_ARG, "range [%lld, %lld) is not inside [0, N = %lld)", (long long)lo,
-                    (long long)hi, (long long)ctx->n);
-    if (lo == hi) return ZG_OK;
-    if (!out) return fail(ZG_ERR_INVALID_ARG, "out is NULL");
-    if (!aligned16(out)) return fail(ZG_ERR_MISALIGNED, "out must be 16-byte aligned");
+    if (int rc = check_gather(ctx, lo, hi, out)) return rc == kNothingToDo ? ZG_OK : rc;
     if (int rc = check_rank_ptrs(ctx, shards, "shards", true)) return rc;
     return finish_launch(zg::launch_gather(ctx->p, ctx->s, shards, lo, hi, out, stream), "parameter gather launch");
 }
@@ -438,13 +449,7 @@ int zg_gather_params(const zg_ctx *ctx, const uint16_t *const *shards, int64_t l
 int zg_gather_params_dma(const zg_ctx *ctx, const uint16_t *const *shards, int64_t lo, int64_t hi, uint16_t *out,
                          zg_stream stream)
 {
-    if (int rc = check_ctx(ctx, false)) return rc;
-    if (lo < 0 || hi < lo || hi > ctx->n)
-        return fail(ZG_ERR_INVALID_ARG, "range [%lld, %lld) is not inside [0, N = %lld)", (long long)lo,
-                    (long long)hi, (long long)ctx->n);
-    if (lo == hi) return ZG_OK;
-    if (!out) return fail(ZG_ERR_INVALID_ARG, "out is NULL");
-    if (!aligned16(out)) return fail(ZG_ERR_MISALIGNED, "out must be 16-byte aligned");
+    if (int rc = check_gather(ctx, lo, hi, out)) return rc == kNothingToDo ? ZG_OK : rc;
     if (int rc = check_rank_ptrs(ctx, shards, "shards", true)) return rc;
     // one device-to-device copy per shard the range crosses (at most P)
     for (int64_t i = lo; i < hi;) {
@@ -461,13 +466,7 @@ int zg_gather_params_dma(const zg_ctx *ctx, const uint16_t *const *shards, int64
 int zg_gather_params_mxfp8(const zg_ctx *ctx, const uint8_t *const *codes, const uint8_t *const *scales, int64_t lo,
                            int64_t hi, uint16_t *out, zg_stream stream)
 {
-    if (int rc = check_ctx(ctx, false)) return rc;
-    if (lo < 0 || hi < lo || hi > ctx->n)
-        return fail(ZG_ERR_INVALID_ARG, "range [%lld, %lld) is not inside [0, N = %lld)", (long long)lo,
-                    (long long)hi, (long long)ctx->n);
-    if (lo == hi) return ZG_OK;
-    if (!out) return fail(ZG_ERR_INVALID_ARG, "out is NULL");
-    if (!aligned16(out)) return fail(ZG_ERR_MISALIGNED, "out must be 16-byte aligned");
+    if (int rc = check_gather(ctx, lo, hi, out)) return rc == kNothingToDo ? ZG_OK : rc;
     if (int rc = check_rank_ptrs(ctx, codes, "codes", true)) return rc;
     if (int rc = check_rank_ptrs(ctx, scales, "scales", false)) return rc;
     return finish_launch(zg::launch_gather_mx(ctx->p, ctx->s, codes, scales, lo, hi, out, stream),

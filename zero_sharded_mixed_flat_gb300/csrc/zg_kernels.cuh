@@ -13,7 +13,9 @@
 //   mh = m/bc1; vh = v/bc2; d = sqrt(vh) + eps
 //   w = w - (lr*wd)*w; w = w - lr*(mh/d); p = bf16_rne(w)
 // (Zero From Scratch, items 3, 6 and 7; the AdamW form is the textbook one
-// with decoupled weight decay, the pages print no formula.)
+// with decoupled weight decay, the pages print no formula.) The one fused
+// multiply-add is in the MXFP8 decode, where each product E4M3 * 2^(s - 127)
+// is exact, so fusing it with the rank sum changes no bit (MxSrc::reduce).
 #pragma once
 
 #include <cuda_bf16.h>
