@@ -248,7 +248,7 @@ def oracle_threaded_steps(workload, ns: int, k: int, ex, threads: int) -> tuple:
     rank's encode per range first), the fp64 partials added in range order,
     one decision, AdamW per range. Same arithmetic as the one-thread oracle;
     the sum of squares differs only by fp64 rounding order. Returns (seconds,
-    w, m, v, t)."""
+    w, m, v, t, the sums of squares of the steps)."""
     import numpy as np
 
     import oracle
@@ -280,17 +280,19 @@ def oracle_threaded_steps(workload, ns: int, k: int, ex, threads: int) -> tuple:
         a, b = ranges[i]
         oracle.adamw_range(hp, dec, res[i][0], w[a:b], m[a:b], v[a:b])
 
+    sums = []
     t0 = time.perf_counter()
     for _ in range(k):
         res = list(ex.map(part, ranges))
         total = 0.0
         for _, ss in res:
             total = total + ss
+        sums.append(total)
         dec, nxt = oracle.decide(hp, t, b1p, b2p, total)
         if not dec.found_inf:
             list(ex.map(lambda i: update(i, dec, res), range(len(ranges))))
             t, b1p, b2p = nxt
-    return time.perf_counter() - t0, w, m, v, t
+    return time.perf_counter() - t0, w, m, v, t, sums
 
 
 def time_oracle_threads(workload, budget_s: float, steps: int, threads: int, warmup: int = 0) -> dict:

@@ -93,10 +93,11 @@ def test_threaded_oracle_matches_the_oracle():
     wl = synth.workload("flat65k_p4")
     ns = 65_536
     with ThreadPoolExecutor(4) as ex:
-        _, w, m, v, t = bench.oracle_threaded_steps(wl, ns, 3, ex, 4)
+        _, w, m, v, t, sums = bench.oracle_threaded_steps(wl, ns, 3, ex, 4)
     ref = oracle.OracleOptimizer(synth.init_weights(wl, 0, ns))
     g = [synth.grads_bf16(wl, 1, r, 0, ns) for r in range(wl.p)]
-    for _ in range(3):
+    for k in range(3):
         dec = ref.step(g, wl.loss_scale)
+        assert abs(sums[k] - dec.sumsq) <= 1e-15 * dec.sumsq  # fp64 summation order only
     assert dec.clip == 1.0 and t == ref.t == 3
     assert w.tobytes() == ref.w.tobytes() and m.tobytes() == ref.m.tobytes() and v.tobytes() == ref.v.tobytes()
