@@ -517,6 +517,35 @@ def pin_gather_mx_vs_torch(lib):
         assert np.array_equal(oracle.gather_mx(codes, scales, s, lo, hi, lib=lib), ref[lo:hi]), (lo, hi)
 
 
+def pin_mx_reduce_vs_torch_decode(lib):
+    """The MX reduce-scatter: each rank's codes decoded through torch's
+    float8_e4m3fn values and an exact power-of-two scaling, added in rank
+    order in binary32 (numpy), then unscaled; bit for bit."""
+    import torch
+
+    rng = np.random.default_rng(29)
+    n, p = 4096, 5
+    codes, scales, vals = [], [], []
+    for _ in range(p):
+        c = rng.integers(0, 256, n).astype(np.uint8)
+        c[(c & 0x7F) == 0x7F] = 0x21  # finite codes only
+        sc = rng.integers(100, 150, n // 32).astype(np.uint8)
+        sc[rng.choice(n // 32, 6, replace=False)] = 0  # subnormal scale
+        codes.append(c)
+        scales.append(sc)
+        v = torch.from_numpy(c).view(torch.float8_e4m3fn).float().numpy().astype(np.float64)
+        vals.append(np.ldexp(v, np.repeat(sc.astype(np.int64) - 127, 32)).astype(np.float32))
+    acc = np.zeros(n, np.float32)
+    for v in vals:
+        acc = (acc + v).astype(np.float32)
+    inv = np.float32(1.0 / (1024.0 * p))
+    want = (acc * inv).astype(np.float32)
+    got = oracle.mx_reduce_unscale(codes, scales, 0, n, float(inv), lib=lib)
+    assert got.tobytes() == want.tobytes()
+    got = oracle.mx_reduce_unscale(codes, scales, 100, 3000, float(inv), lib=lib)
+    assert got.tobytes() == want[100:3000].tobytes()
+
+
 PINS = [
     pin_first_step_closed_form,
     pin_first_step_weight_decay,
@@ -539,6 +568,7 @@ PINS = [
     pin_gather_owner_offset,
     pin_gather_mx_hand_values,
     pin_gather_mx_vs_torch,
+    pin_mx_reduce_vs_torch_decode,
 ]
 
 

@@ -49,6 +49,8 @@ MUTANTS = {
     "mx_f32_through_bf16": ("vals[j] = (double)x[lo + j];",
                             "vals[j] = (double)orc_bf16_to_f32(orc_f32_to_bf16(x[lo + j]));"),
     "shard_not_block_aligned": ("return (s + 31) / 32 * 32;", "return s;"),
+    "mx_reduce_scale_of_next_rank": ("s = s + orc_mx_decode(codes[r][i], scales[r][i / 32]);",
+                                     "s = s + orc_mx_decode(codes[r][i], scales[(r + 1) % p][i / 32]);"),
     "gather_neighbour_offset": ("out[i - lo] = shards[r][k];", "out[i - lo] = shards[r][k ^ 1];"),
     "gather_from_rank_zero": ("out[i - lo] = shards[r][k];", "out[i - lo] = shards[0][k];"),
     "gather_mx_scale_of_rank_zero": ("scales[r][k / 32]", "scales[0][k / 32]"),
