@@ -546,6 +546,40 @@ def pin_mx_reduce_vs_torch_decode(lib):
     assert got.tobytes() == want[100:3000].tobytes()
 
 
+def pin_mx_step_lossless_equals_bf16_step(lib):
+    """Gradients whose every value is exactly an E4M3 value times its block's
+    scale (each block's values are +-(1 + k/8) 2^j, k <= 6, within six binades
+    of the block maximum, which has the block's top exponent) encode without loss,
+    so the MX step must equal the bf16 step on the same values bit for bit."""
+    rng = np.random.default_rng(31)
+    n, p, L = 4096, 3, 1024.0
+
+    def lossless(seed):
+        r = np.random.default_rng(seed)
+        x = np.empty(n, np.float32)
+        for b in range(n // 32):
+            top = int(r.integers(-5, 3))
+            k = r.integers(0, 7, 32)  # E4M3's top binade ends at 1.75 (mantissa 111 there is NaN)
+            d = r.integers(0, 7, 32)
+            d[0] = 0  # one value carries the block's top exponent
+            x[32 * b:32 * b + 32] = (r.choice([-1.0, 1.0], 32) * (1 + k / 8) * 2.0 ** (top - d)).astype(np.float32)
+        return _bf16(x)
+
+    w0 = (rng.standard_normal(n) * 0.02).astype(np.float32)
+    a, b = _opt(lib, w0), _opt(lib, w0)
+    for t in range(3):
+        grads = [lossless(100 * t + r) for r in range(p)]
+        enc = [oracle.mx_encode(g, lib=lib) for g in grads]
+        for g, (c, sc) in zip(grads, enc):  # the encoding is lossless
+            dec = np.array([oracle.mx_decode(c[i], sc[i // 32], lib=lib) for i in range(0, n, 97)], np.float32)
+            assert np.array_equal(dec, (g[::97].astype(np.uint32) << 16).view(np.float32))
+        da = a.step(grads, L)
+        db = b.step_mx([c for c, _ in enc], [sc for _, sc in enc], L)
+        assert da.sumsq == db.sumsq and da.clip == db.clip
+    for x, y in ((a.w, b.w), (a.m, b.m), (a.v, b.v), (a.p, b.p)):
+        assert x.tobytes() == y.tobytes()
+
+
 PINS = [
     pin_first_step_closed_form,
     pin_first_step_weight_decay,
@@ -569,6 +603,7 @@ PINS = [
     pin_gather_mx_hand_values,
     pin_gather_mx_vs_torch,
     pin_mx_reduce_vs_torch_decode,
+    pin_mx_step_lossless_equals_bf16_step,
 ]
 
 
