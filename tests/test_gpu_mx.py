@@ -135,3 +135,40 @@ def test_mx_step_raw_bytes():
         assert bool(dec.found_inf) == (k in (2, 3)), (k, dec.found_inf)
         check_step(f"mx-raw step {k + 1}", run, ref, dec, info, k + 1)
     assert ref.t == 3
+
+
+def _lossless_bf16(n: int, seed: int) -> np.ndarray:
+    """bf16 values every one of which MXFP8 encodes exactly: per 32-block,
+    +-(1 + k/8) 2^j with k <= 6 and j within six binades of the block's top
+    exponent, which one value carries."""
+    r = np.random.default_rng(seed)
+    x = np.empty(n, np.float32)
+    for b in range(0, n, 32):
+        m = min(32, n - b)
+        top = int(r.integers(-8, 4))
+        d = r.integers(0, 7, m)
+        d[0] = 0
+        x[b:b + m] = r.choice([-1.0, 1.0], m) * (1 + r.integers(0, 7, m) / 8) * 2.0 ** (top - d)
+    return (x.view(np.uint32) >> 16).astype(np.uint16)
+
+
+@pytest.mark.parametrize("n,p", [(4099, 4), ((1 << 20) + 96, 8)])
+def test_mx_step_on_lossless_gradients_equals_bf16_step(n, p):
+    """Encoded on the GPU, gradients MXFP8 holds exactly must give the MX step
+    the bf16 step's bits (the two decode paths meet on the same fp32 values)."""
+    w0 = (np.random.default_rng(n).standard_normal(n) * 0.02).astype(np.float32)
+    a, b = GpuRun(w0, p), GpuRun(w0, p)
+    for t in range(3):
+        host = [_lossless_bf16(n, 1000 * t + r) for r in range(p)]
+        dev = [to_dev_bf16(h) for h in host]
+        codes = [torch.empty(n, dtype=torch.uint8, device="cuda") for _ in range(p)]
+        scales = [torch.empty((n + 31) // 32, dtype=torch.uint8, device="cuda") for _ in range(p)]
+        for r in range(p):
+            zb.zg_quant_mxfp8(dev[r], codes[r], scales[r], n)
+        zb.zg_step(a.ctx, dev, 1024.0)
+        zb.zg_step_mxfp8(b.ctx, codes, scales, 1024.0)
+        ia, ib = zb.zg_get_info(a.ctx), zb.zg_get_info(b.ctx)
+        assert ia.status == ib.status == 0 and ia.sumsq == ib.sumsq and ia.clip_coef == ib.clip_coef, (t, ia, ib)
+    sa, sb = a.state(), b.state()
+    for k in sa:
+        assert sa[k].tobytes() == sb[k].tobytes(), k
