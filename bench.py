@@ -792,28 +792,30 @@ def bench_ours(args, rank: int, world: int, local: int) -> dict | None:
     # here and parked in host memory, as a sending rank would transmit them).
     e2e = None
     if not args.no_e2e:
+        # the P ranks' inputs sit end to end in one pinned buffer and one
+        # device slot, so a step's host-to-device transfer is one copy per array
         if wl.mx:
             for r in range(p):
                 zb.zg_quant_mxfp8(dev[r], codes[r], scales[r], n, stream)
-            slots = [(codes, scales),
-                     ([torch.empty_like(c) for c in codes], [torch.empty_like(s) for s in scales])]
-            h_in = [c[:n].cpu().pin_memory() for c in codes] + [s[:(n + 31) // 32].cpu().pin_memory() for s in scales]
-
-            def slot_inputs(k):
-                c, s = slots[k]
-                return [x[:n] for x in c] + [x[:(n + 31) // 32] for x in s]
-
-            def step_on(k):
-                zb.zg_step_mxfp8(opt.ctx, slots[k][0], slots[k][1], ls, stream)
-        else:
-            slots = [dev, [torch.empty_like(d) for d in dev]]
-            h_in = [h.pin_memory() for h in host_t]
+            # rows of the padded length P * S (a multiple of 32): every rank's codes stay 16-byte aligned
+            h_in = [torch.stack(codes).cpu().pin_memory(), torch.stack(scales).cpu().pin_memory()]
+            slots = [[torch.empty_like(h, device="cuda") for h in h_in] for _ in range(2)]
 
             def slot_inputs(k):
                 return slots[k]
 
             def step_on(k):
-                zb.zg_step(opt.ctx, slots[k], ls, stream)
+                c, sc = slots[k]
+                zb.zg_step_mxfp8(opt.ctx, list(c.unbind(0)), list(sc.unbind(0)), ls, stream)
+        else:
+            h_in = [torch.stack(host_t).pin_memory()]
+            slots = [[torch.empty_like(h_in[0], device="cuda")] for _ in range(2)]
+
+            def slot_inputs(k):
+                return slots[k]
+
+            def step_on(k):
+                zb.zg_step(opt.ctx, list(slots[k][0].unbind(0)), ls, stream)
         e2e = time_e2e(h_in, slot_inputs, step_on, opt, stream, max(3, min(K, 200)), world)
         e2e.update(h2d_bytes_per_step=sum(h.numel() * h.element_size() for h in h_in),
                    d2h_bytes_per_step=SCALARS_D2H_BYTES,
