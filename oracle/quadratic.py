@@ -1,4 +1,4 @@
-"""A model small enough to hold in your head, for the gradient check.
+"""A tiny model whose every number can be worked by hand, for the gradient check.
 
 TEST INFRASTRUCTURE ONLY (part of the oracle; see ``oracle/__init__.py``).
 
