@@ -458,6 +458,12 @@ struct NormMinBlocks {
 #endif
 };
 constexpr int kNormFlush = 4;  // vectors (32 elements) per two-sum run before widening to fp64
+// The tail of the staged gradient written with the default store policy (see
+// norm_kernel); the rest uses evict-first stores.
+#ifndef ZG_STAGE_KEEP_MB
+#define ZG_STAGE_KEEP_MB 96
+#endif
+constexpr int64_t kStageKeepBytes = int64_t(ZG_STAGE_KEEP_MB) << 20;
 static_assert(kNormFlush % kNormUnroll == 0, "a run holds whole unrolled groups");
 
 // Finalize: runs once, in the last block of the norm pass (thread 0).
@@ -559,10 +565,22 @@ __global__ void __launch_bounds__(kNormThreads, NormMinBlocks<Src>::value)
                     gh[j] = __fmul_rn(gh[j], inv);
                     two_sum_acc(hi, lo, __fmul_rn(gh[j], gh[j]));
                 }
-                if (kStage) {  // keep the reduce-scatter output for the step pass
-                    float4 *o = reinterpret_cast<float4 *>(stage) + 2 * (v + u * stride);
-                    __stcs(o, make_float4(gh[0], gh[1], gh[2], gh[3]));
-                    __stcs(o + 1, make_float4(gh[4], gh[5], gh[6], gh[7]));
+                if (kStage) {
+                    // keep the reduce-scatter output for the step pass. Its
+                    // last kStageKeepBytes (the part the step pass, walking
+                    // from the end, reads first) get the default store policy
+                    // so they can still be in L2; the rest streams out.
+                    const int64_t vv = v + u * stride;
+                    float4 *o = reinterpret_cast<float4 *>(stage) + 2 * vv;
+                    const float4 a = make_float4(gh[0], gh[1], gh[2], gh[3]);
+                    const float4 b = make_float4(gh[4], gh[5], gh[6], gh[7]);
+                    if (vv >= nvec - kStageKeepBytes / 32) {
+                        o[0] = a;
+                        o[1] = b;
+                    } else {
+                        __stcs(o, a);
+                        __stcs(o + 1, b);
+                    }
                 }
             }
         }

@@ -106,10 +106,17 @@ __global__ void __launch_bounds__(kNormThreads, MxNormMinBlocks<P>::value)
                 g[j] = gg.x;
                 g[j + 1] = gg.y;
             }
-            if (kStage) {
+            if (kStage) {  // the tail the step pass reads first keeps the default policy
                 float4 *o = reinterpret_cast<float4 *>(stage) + 4 * v;
+                const bool keep = v >= nvec - kStageKeepBytes / 64;
 #pragma unroll
-                for (int q = 0; q < 4; ++q) __stcs(o + q, make_float4(g[4 * q], g[4 * q + 1], g[4 * q + 2], g[4 * q + 3]));
+                for (int q = 0; q < 4; ++q) {
+                    const float4 x = make_float4(g[4 * q], g[4 * q + 1], g[4 * q + 2], g[4 * q + 3]);
+                    if (keep)
+                        o[q] = x;
+                    else
+                        __stcs(o + q, x);
+                }
             }
         }
         if (isfinite(hi) && isfinite(lo)) {
