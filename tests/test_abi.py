@@ -70,3 +70,29 @@ def test_no_cpu_fallback_without_a_gpu(lib):
     with pytest.raises(zb.ZgError) as e:
         zb.zg_init(1024, 4)
     assert e.value.code == zb.ZG_ERR_CUDA
+
+
+def test_binding_refuses_host_tensors_before_any_call():
+    """Every device-pointer argument is checked in the binding: a host tensor
+    (or a non-tensor) never reaches the library as an address."""
+    import torch
+
+    host_bf16 = torch.zeros(64, dtype=torch.bfloat16)
+    host_u8 = torch.zeros(64, dtype=torch.uint8)
+    host_f64 = torch.zeros(2, dtype=torch.float64)
+    with pytest.raises(TypeError, match="src must be a CUDA tensor"):
+        zb.zg_probe_copy(torch.zeros(16), torch.zeros(16))
+    with pytest.raises(TypeError, match="src must be a tensor"):
+        zb.zg_probe_copy(12345, torch.zeros(16))
+    with pytest.raises(TypeError, match="in must be a CUDA tensor"):
+        zb.zg_quant_mxfp8(host_bf16, host_u8, host_u8)
+    with pytest.raises(TypeError, match=r"grads\[0\] must be a CUDA tensor"):
+        zb.zg_grad_norm_noalloc([host_bf16], 64, 1.0, host_f64)
+    ctx = zb.Ctx(None, 64, 2)  # a handle is never reached: the checks come first
+    with pytest.raises(TypeError, match=r"grads\[0\] must be a CUDA tensor"):
+        zb.zg_step(ctx, [host_bf16, host_bf16], 1.0)
+    with pytest.raises(ValueError, match="expected 2 gradient buffers"):
+        zb.zg_step(ctx, [host_bf16], 1.0)
+    with pytest.raises(TypeError, match="w must be a CUDA tensor or pinned host memory"):
+        zb.zg_bind(ctx, torch.zeros(64), torch.zeros(64), torch.zeros(64), host_bf16)
+

@@ -320,10 +320,14 @@ def zg_set_wait_limit(ctx: Ctx, polls: int) -> None:
 
 
 def zg_probe_copy(src: torch.Tensor, dst: torch.Tensor, stream=None) -> None:
-    nbytes = src.numel() * src.element_size()
+    """Copy src's bytes into dst with the library's streaming copy kernel
+    (both CUDA tensors, contiguous; any dtype, byte count a multiple of 16)."""
+    nbytes = src.numel() * src.element_size() if isinstance(src, torch.Tensor) else 0
+    s = _dev_ptr(src, src.dtype if isinstance(src, torch.Tensor) else None, 0, "src")
+    d = _dev_ptr(dst, dst.dtype if isinstance(dst, torch.Tensor) else None, 0, "dst")
     if dst.numel() * dst.element_size() < nbytes:
         raise ValueError("dst smaller than src")
-    _check(lib().zg_probe_copy(src.data_ptr(), dst.data_ptr(), nbytes, _stream(stream)), "zg_probe_copy")
+    _check(lib().zg_probe_copy(s, d, nbytes, _stream(stream)), "zg_probe_copy")
 
 
 def zg_grad_norm_noalloc(grads, n: int, loss_scale: float, out: torch.Tensor, grad_average: int = 1,
