@@ -95,7 +95,8 @@ typedef struct {
 
 /* Create a context for N parameters over P simulated ranks (1 <= P <= 16,
  * 1 <= N < 2^62) on the current CUDA device. Allocates only a small device
- * workspace (a few KB: the norm pass's block partials and the step scalars).
+ * workspace (64 KB of fp64 norm-pass block partials and a 112-byte block of
+ * step scalars).
  * Step count starts at 0. Layout: Zero From Scratch, item 17 (one flat
  * vector cut into P contiguous shards). *out is NULL on failure. */
 int zg_init(int64_t n, int p, const zg_hparams *hp, zg_ctx **out);
