@@ -116,3 +116,59 @@ def test_random_combination_matches_oracle(seed):
         assert run.guards_intact(), seed
     log({"case": "random-combo", "seed": seed, **{k: v for k, v in c.items() if k != "hp"}, **c["hp"],
          "t": ref.t})
+
+
+BUCKET_CASES = 60
+
+
+def draw_buckets(seed: int) -> dict:
+    """N, P, variant and a random partition of [0, N) into contiguous buckets
+    whose inner edges are multiples of 8 (the bucket entry point's rule)."""
+    rng = np.random.default_rng(0xB0C4E7 + seed)
+    n = int(round(np.exp(rng.uniform(0, np.log(3e5)))))
+    inner = np.arange(8, n, 8)
+    k = int(min(inner.size, rng.integers(0, 12)))
+    cuts = sorted(rng.choice(inner, size=k, replace=False).tolist()) if k else []
+    edges = [0] + cuts + [n]
+    return {"n": n, "p": int(rng.integers(1, 17)), "variant": str(rng.choice(["ldg", "tma", "staged"])),
+            "buckets": list(zip(edges[:-1], edges[1:])), "plant": bool(rng.integers(0, 4) == 0),
+            "plant_at": float(rng.uniform())}
+
+
+@pytest.mark.parametrize("seed", range(BUCKET_CASES),
+                         ids=lambda s: f"{s}-n{draw_buckets(s)['n']}-b{len(draw_buckets(s)['buckets'])}")
+def test_random_bucket_partition_matches_oracle(seed):
+    """The norm taken over a random bucket partition equals the whole-vector
+    norm (same squares, fp64 sums associated per bucket: 1e-12), and the step
+    that follows matches the oracle."""
+    c = draw_buckets(seed)
+    n, p, L = c["n"], c["p"], 1024.0
+    w0 = (np.random.default_rng(seed + 77).standard_normal(n) * 0.02).astype(np.float32)
+    run, whole = GpuRun(w0, p), GpuRun(w0, p)
+    ref = oracle.OracleOptimizer(w0)
+    if c["variant"] == "staged":
+        stage = torch.zeros(n, dtype=torch.float32, device="cuda")
+        zb.zg_bind_grad_stage(run.ctx, stage)
+        zb.zg_set_variant(run.ctx, zb.ZG_VARIANT_STAGED)
+    elif c["variant"] == "tma":
+        zb.zg_set_variant(run.ctx, zb.ZG_VARIANT_TMA)
+    for k in range(STEPS):
+        host = [synth.random_bf16(n, seed=190_000 + 1000 * seed + 10 * k + r, scale=(1e-3 if k != 1 else 0.3) * L)
+                for r in range(p)]
+        if k == 2 and c["plant"]:
+            host[int(c["plant_at"] * p)][int(c["plant_at"] * n)] = 0x7F80
+        dev = [to_dev_bf16(h) for h in host]
+        last = len(c["buckets"]) - 1
+        for i, (lo, hi) in enumerate(c["buckets"]):
+            flags = (zb.ZG_BUCKET_FIRST if i == 0 else 0) | (zb.ZG_BUCKET_LAST if i == last else 0)
+            zb.zg_grad_norm_bucket(run.ctx, dev, lo, hi, L, flags)
+        zb.zg_grad_norm(whole.ctx, dev, L)
+        a, b = zb.zg_get_info(run.ctx), zb.zg_get_info(whole.ctx)
+        assert a.found_inf == b.found_inf, (seed, k)
+        if not b.found_inf:
+            assert abs(a.sumsq - b.sumsq) <= 1e-12 * b.sumsq, (seed, k, a.sumsq, b.sumsq)
+        zb.zg_shard_step(run.ctx, dev, L)
+        zb.zg_shard_step(whole.ctx, dev, L)
+        dec = ref.step(host, L)
+        check_step(f"random buckets {seed}", run, ref, dec, zb.zg_get_info(run.ctx), k + 1)
+        assert run.guards_intact(), seed
