@@ -13,6 +13,8 @@ What pins what:
     lr * g / (|g| + eps);
   - weight decay closed form: w (1 - lr wd) - lr g / (|g| + eps);
   - two-step closed form with two different gradients, written out;
+  - the clip + AdamW chain against torch.nn.utils.clip_grad_norm_ and
+    torch.optim.AdamW (another rounding order, so to rounding);
   - clip: a vector of one repeated value has norm |a| sqrt(N);
   - norm: index-order binary64 sum vs math.fsum (correctly rounded);
   - averaging and loss scale on integer-valued gradients (exact);
@@ -143,6 +145,50 @@ def pin_two_step_closed_form(lib):
 
 
 # ------------------------------------------------------------- clip and norm
+
+def pin_adamw_and_clip_vs_torch(lib):
+    """The whole clip + AdamW chain against PyTorch's own implementation of
+    the same algorithm (torch.nn.utils.clip_grad_norm_, whose coefficient is
+    max_norm / (norm + 1e-6) clamped to 1, then torch.optim.AdamW, single-tensor
+    path): one rank, loss scale 1, so the oracle's gradient is the bf16 value
+    itself. PyTorch rounds in another order (a lerp for m, sqrt(v) / sqrt(bc2)
+    for the denominator, its norm in binary32), so the two agree to rounding,
+    over steps that clip and steps that do not; a wrong beta, sign, bias
+    correction, eps placement, clip rule or decay form shows as a large error."""
+    import torch
+
+    rng = np.random.default_rng(20)
+    n = 4096
+    hp = oracle.Hparams()
+    w0 = (rng.standard_normal(n) * 0.02).astype(np.float32)
+    ref = _opt(lib, w0)
+    param = torch.nn.Parameter(torch.from_numpy(w0.copy()))
+    topt = torch.optim.AdamW([param], lr=hp.lr, betas=(hp.beta1, hp.beta2), eps=hp.eps,
+                             weight_decay=hp.weight_decay, foreach=False)
+    clipped = unclipped = 0
+    for t, sigma in enumerate((1e-3, 0.05, 2e-3, 0.1, 1e-3, 0.03)):
+        g = _trunc(rng.standard_normal(n).astype(np.float32) * np.float32(sigma))
+        dec = ref.step([g], 1.0)
+        param.grad = torch.from_numpy((g.astype(np.uint32) << 16).view(np.float32).copy())
+        total = float(torch.nn.utils.clip_grad_norm_([param], hp.max_grad_norm))
+        topt.step()
+        assert abs(dec.norm - total) <= 1e-6 * total
+        clipped += dec.clip < 1.0
+        unclipped += dec.clip == 1.0
+    assert clipped >= 2 and unclipped >= 2
+    # Two rounding orders differ by a few binary32 ulps of the intermediate
+    # terms, which is hundreds of ulps of a result that cancels to near zero
+    # (m changing sign, w crossing zero): bound the difference by the array's
+    # RMS (measured at most 7e-6 of it) and the typical element's relative
+    # error (measured 1e-7 to 8e-7). A dropped weight decay already moves w by
+    # about 6e-5 of its RMS over these steps.
+    st = topt.state[param]
+    for mine, theirs in ((ref.w, param.detach()), (ref.m, st["exp_avg"]), (ref.v, st["exp_avg_sq"])):
+        theirs = theirs.numpy().astype(np.float64)
+        diff = np.abs(mine.astype(np.float64) - theirs)
+        assert diff.max() <= 2e-5 * np.sqrt(np.mean(theirs * theirs)), diff.max()
+        assert np.median(diff / np.maximum(np.abs(theirs), 1e-30)) <= 2e-6
+
 
 def pin_clip_constant_vector(lib):
     """Every gradient element a: the norm is |a| sqrt(N)."""
@@ -585,6 +631,7 @@ PINS = [
     pin_first_step_weight_decay,
     pin_constant_gradient,
     pin_two_step_closed_form,
+    pin_adamw_and_clip_vs_torch,
     pin_clip_constant_vector,
     pin_norm_vs_fsum,
     pin_average_and_unscale,
