@@ -959,13 +959,19 @@ cudaError_t with_ranks(int p, F &&f)
 // The same fused step, with the operands of each 2048-element tile staged
 // in shared memory by 1-D bulk asynchronous copies (cp.async.bulk, global to
 // this CTA's shared memory, completion counted in bytes on an mbarrier): P
-// bf16 gradient slices and the fp32 w, m, v. One CTA per SM walks its tiles
-// through a ring of `stages` buffers; thread 0 refills a buffer as soon as
-// every thread has finished reading it. Results go straight from registers
-// to HBM with 128-bit streaming stores.
+// bf16 gradient slices and the fp32 w, m, v. The CTA is warp-specialised:
+// one producer warp walks the CTA's tiles through a ring of `stages`
+// buffers, and eight consumer warps (8 elements per thread per tile) read a
+// buffer into registers, release it and compute. Each buffer has a "full"
+// barrier (the producer's expect_tx arrival plus the copied bytes) and an
+// "empty" barrier (one arrival per consumer warp), so no block-wide barrier
+// sits in the tile loop and the producer refills a buffer as soon as the
+// last warp has read it. Results go straight from registers to HBM with
+// 128-bit streaming stores.
 //
-// Every wait is bounded (`wait_limit` polls). A wait that runs out records
-// the timeout, waits (bounded again) for the copies this CTA already issued,
+// Every wait is bounded (`wait_limit` polls) and gives up early once another
+// thread of the CTA has recorded a timeout. A wait that runs out records the
+// timeout, the CTA waits (bounded again) for the copies it already issued,
 // skips the rest of its work and returns; the step is then not committed.
 
 namespace zg {
@@ -1047,14 +1053,39 @@ struct Layout {
     }
 };
 
+constexpr int kConsumers = kThreads;        // 8 elements per consumer thread per tile
+constexpr int kWsThreads = kConsumers + 32;  // plus the producer warp
+#ifndef ZG_TMA_WS_MINB
+#define ZG_TMA_WS_MINB 1
+#endif
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+// Bounded wait that also gives up once another thread of the CTA has
+// recorded a timeout (checked every 256 polls).
+__device__ __forceinline__ bool mbar_wait_or_abort(uint64_t *bar, uint32_t parity, long long limit,
+                                                   const volatile int *abort)
+{
+    for (long long i = 0; i < limit; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 255) == 255 && *abort) return false;
+    }
+    return false;
+}
+
 template <int P>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kWsThreads, ZG_TMA_WS_MINB)
     step_kernel_tma(Bf16Src<P> src, int64_t n, float inv, StepK k, State st, Scalars *sc, int stages,
                     long long wait_limit)
 {
     extern __shared__ __align__(128) unsigned char smem[];
-    __shared__ __align__(8) uint64_t bars[8];
+    __shared__ __align__(8) uint64_t full[8];
+    __shared__ __align__(8) uint64_t empty[8];
     __shared__ int s_timeout;
+    __shared__ long long s_issued;
 
     pdl_wait();
     pdl_trigger();
@@ -1068,7 +1099,11 @@ __global__ void __launch_bounds__(kThreads)
 
     if (threadIdx.x == 0) {
         s_timeout = 0;
-        for (int s = 0; s < stages; ++s) mbar_init(&bars[s], 1);
+        s_issued = 0;
+        for (int s = 0; s < stages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kConsumers / 32);
+        }
         fence_barrier_init();
     }
     __syncthreads();
@@ -1080,91 +1115,106 @@ __global__ void __launch_bounds__(kThreads)
         const int64_t t = int64_t(blockIdx.x) + j * gridDim.x;
         return (ZG_TMA_REVERSE ? ntiles - 1 - t : t) * kTile;
     };
-    auto issue = [&](int64_t j) {  // thread 0: start the copies of this CTA's j-th tile
-        const int s = int(j % stages);
-        const int64_t t0 = tile_start(j);
-        const int64_t len = covered - t0 < kTile ? covered - t0 : kTile;
-        unsigned char *buf = stage_ptr(s);
-        const uint32_t gb = uint32_t(len * 2), fb = uint32_t(len * 4);
-        mbar_expect_tx(&bars[s], P * gb + 3 * fb);
-#pragma unroll
-        for (int r = 0; r < P; ++r) bulk_g2s(buf + r * lay.grad_bytes, src.g[r] + t0, gb, &bars[s]);
-        float *f = reinterpret_cast<float *>(buf + P * lay.grad_bytes);
-        bulk_g2s(f, st.w + t0, fb, &bars[s]);
-        bulk_g2s(f + kTile, st.m + t0, fb, &bars[s]);
-        bulk_g2s(f + 2 * kTile, st.v + t0, fb, &bars[s]);
-    };
+    const volatile int *abort = &s_timeout;
+    const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
 
-    int64_t issued = 0;
-    if (skip == 0 && threadIdx.x == 0)
-        for (; issued < my_tiles && issued < stages; ++issued) issue(issued);
-
-    bool timed_out = false;
-    int64_t consumed = 0;
-    for (int64_t j = 0; skip == 0 && j < my_tiles; ++j, consumed = j) {
-        const int s = int(j % stages);
-        const uint32_t parity = uint32_t((j / stages) & 1);
-        if (!mbar_wait(&bars[s], parity, wait_limit)) timed_out = true;
-        if (timed_out) atomicExch(&s_timeout, 1);
-        __syncthreads();
-        if (s_timeout) break;
-        const int64_t t0 = tile_start(j);
-        const int64_t len = covered - t0 < kTile ? covered - t0 : kTile;
-        const int e = threadIdx.x * kVec;
-        if (e < len) {
-            const unsigned char *buf = stage_ptr(s);
-            float gh[kVec];
+    if (skip == 0 && warp == kConsumers / 32) {
+        // producer: one lane issues every copy of this CTA's tiles in order
+        if (lane == 0) {
+            int64_t j = 0;
+            for (; j < my_tiles; ++j) {
+                const int s = int(j % stages);
+                if (j >= stages &&
+                    !mbar_wait_or_abort(&empty[s], uint32_t(((j / stages) - 1) & 1), wait_limit, abort)) {
+                    atomicExch(&s_timeout, 1);
+                    break;
+                }
+                const int64_t t0 = tile_start(j);
+                const int64_t len = covered - t0 < kTile ? covered - t0 : kTile;
+                unsigned char *buf = stage_ptr(s);
+                const uint32_t gb = uint32_t(len * 2), fb = uint32_t(len * 4);
+                mbar_expect_tx(&full[s], P * gb + 3 * fb);
 #pragma unroll
-            for (int q = 0; q < kVec; ++q) gh[q] = 0.0f;
+                for (int r = 0; r < P; ++r) bulk_g2s(buf + r * lay.grad_bytes, src.g[r] + t0, gb, &full[s]);
+                float *f = reinterpret_cast<float *>(buf + P * lay.grad_bytes);
+                bulk_g2s(f, st.w + t0, fb, &full[s]);
+                bulk_g2s(f + kTile, st.m + t0, fb, &full[s]);
+                bulk_g2s(f + 2 * kTile, st.v + t0, fb, &full[s]);
+            }
+            s_issued = j;
+        }
+    } else if (skip == 0) {
+        for (int64_t j = 0; j < my_tiles; ++j) {
+            const int s = int(j % stages);
+            // one decision per warp, so no lane leaves while the others sync
+            const bool ok = __all_sync(0xffffffffu, mbar_wait_or_abort(&full[s], uint32_t((j / stages) & 1),
+                                                                        wait_limit, abort));
+            if (!ok) {
+                if (lane == 0) atomicExch(&s_timeout, 1);
+                break;
+            }
+            const int64_t t0 = tile_start(j);
+            const int64_t len = covered - t0 < kTile ? covered - t0 : kTile;
+            const int e = threadIdx.x * kVec;
+            const bool active = e < len;
+            float gh[kVec], w[kVec], m[kVec], v[kVec];
+            if (active) {
+                const unsigned char *buf = stage_ptr(s);
 #pragma unroll
-            for (int r = 0; r < P; ++r) {
-                const uint4 x = *reinterpret_cast<const uint4 *>(buf + r * lay.grad_bytes + e * 2);
-                const uint32_t w4[4] = {x.x, x.y, x.z, x.w};
+                for (int q = 0; q < kVec; ++q) gh[q] = 0.0f;
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    gh[2 * q] = __fadd_rn(gh[2 * q], bf16_lo(w4[q]));
-                    gh[2 * q + 1] = __fadd_rn(gh[2 * q + 1], bf16_hi(w4[q]));
+                for (int r = 0; r < P; ++r) {
+                    const uint4 x = *reinterpret_cast<const uint4 *>(buf + r * lay.grad_bytes + e * 2);
+                    const uint32_t w4[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        gh[2 * q] = __fadd_rn(gh[2 * q], bf16_lo(w4[q]));
+                        gh[2 * q + 1] = __fadd_rn(gh[2 * q + 1], bf16_hi(w4[q]));
+                    }
+                }
+                const float *f = reinterpret_cast<const float *>(buf + P * lay.grad_bytes);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const float4 a = *reinterpret_cast<const float4 *>(f + e + 4 * h);
+                    const float4 b = *reinterpret_cast<const float4 *>(f + kTile + e + 4 * h);
+                    const float4 d = *reinterpret_cast<const float4 *>(f + 2 * kTile + e + 4 * h);
+                    w[4 * h] = a.x, w[4 * h + 1] = a.y, w[4 * h + 2] = a.z, w[4 * h + 3] = a.w;
+                    m[4 * h] = b.x, m[4 * h + 1] = b.y, m[4 * h + 2] = b.z, m[4 * h + 3] = b.w;
+                    v[4 * h] = d.x, v[4 * h + 1] = d.y, v[4 * h + 2] = d.z, v[4 * h + 3] = d.w;
                 }
             }
-            const float *f = reinterpret_cast<const float *>(buf + P * lay.grad_bytes);
-            float w[kVec], m[kVec], v[kVec];
+            // the warp's reads of buffer s are done: release it before computing
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);
+            if (active) {
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const float4 a = *reinterpret_cast<const float4 *>(f + e + 4 * h);
-                const float4 b = *reinterpret_cast<const float4 *>(f + kTile + e + 4 * h);
-                const float4 d = *reinterpret_cast<const float4 *>(f + 2 * kTile + e + 4 * h);
-                w[4 * h] = a.x, w[4 * h + 1] = a.y, w[4 * h + 2] = a.z, w[4 * h + 3] = a.w;
-                m[4 * h] = b.x, m[4 * h + 1] = b.y, m[4 * h + 2] = b.z, m[4 * h + 3] = b.w;
-                v[4 * h] = d.x, v[4 * h + 1] = d.y, v[4 * h + 2] = d.z, v[4 * h + 3] = d.w;
+                for (int q = 0; q < kVec; ++q) adamw(__fmul_rn(gh[q], inv), c, bc1, bc2, k, w[q], m[q], v[q]);
+                const int64_t gi = t0 + e;
+                float4 *w4 = reinterpret_cast<float4 *>(st.w + gi);
+                float4 *m4 = reinterpret_cast<float4 *>(st.m + gi);
+                float4 *v4 = reinterpret_cast<float4 *>(st.v + gi);
+                st_stream(w4, make_float4(w[0], w[1], w[2], w[3]));
+                st_stream(w4 + 1, make_float4(w[4], w[5], w[6], w[7]));
+                st_stream(m4, make_float4(m[0], m[1], m[2], m[3]));
+                st_stream(m4 + 1, make_float4(m[4], m[5], m[6], m[7]));
+                st_stream(v4, make_float4(v[0], v[1], v[2], v[3]));
+                st_stream(v4 + 1, make_float4(v[4], v[5], v[6], v[7]));
+                st_stream(reinterpret_cast<uint4 *>(st.p + gi),
+                          make_uint4(pack_bf16x2(w[0], w[1]), pack_bf16x2(w[2], w[3]), pack_bf16x2(w[4], w[5]),
+                                     pack_bf16x2(w[6], w[7])));
             }
-#pragma unroll
-            for (int q = 0; q < kVec; ++q) adamw(__fmul_rn(gh[q], inv), c, bc1, bc2, k, w[q], m[q], v[q]);
-            const int64_t gi = t0 + e;
-            float4 *w4 = reinterpret_cast<float4 *>(st.w + gi);
-            float4 *m4 = reinterpret_cast<float4 *>(st.m + gi);
-            float4 *v4 = reinterpret_cast<float4 *>(st.v + gi);
-            st_stream(w4, make_float4(w[0], w[1], w[2], w[3]));
-            st_stream(w4 + 1, make_float4(w[4], w[5], w[6], w[7]));
-            st_stream(m4, make_float4(m[0], m[1], m[2], m[3]));
-            st_stream(m4 + 1, make_float4(m[4], m[5], m[6], m[7]));
-            st_stream(v4, make_float4(v[0], v[1], v[2], v[3]));
-            st_stream(v4 + 1, make_float4(v[4], v[5], v[6], v[7]));
-            st_stream(reinterpret_cast<uint4 *>(st.p + gi),
-                      make_uint4(pack_bf16x2(w[0], w[1]), pack_bf16x2(w[2], w[3]), pack_bf16x2(w[4], w[5]),
-                                 pack_bf16x2(w[6], w[7])));
         }
-        __syncthreads();  // everyone is done reading buffer s
-        if (threadIdx.x == 0 && issued < my_tiles) issue(issued++);
     }
+    __syncthreads();
 
     if (s_timeout) {
-        // Drain: wait (bounded) for every copy this CTA issued and has not
-        // consumed, so no bulk copy lands after the CTA is gone.
+        // Drain: wait (bounded) for the copies still in flight, the last
+        // `stages` tiles issued at most, so no bulk copy lands after the CTA
+        // is gone.
         if (threadIdx.x == 0) {
-            for (int64_t j = consumed; j < issued; ++j) {
-                const int s = int(j % stages);
-                mbar_wait(&bars[s], uint32_t((j / stages) & 1), kDrainLimit);
-            }
+            const int64_t issued = s_issued;
+            for (int64_t j = issued > stages ? issued - stages : 0; j < issued; ++j)
+                mbar_wait(&full[int(j % stages)], uint32_t((j / stages) & 1), kDrainLimit);
             sc->status = kStatusTimeout;
             atomicAdd(&sc->step_faults, 1u);
         }

@@ -3,12 +3,16 @@
 
 namespace zg {
 
+// One warp-specialised CTA per SM with three ring buffers: measured on
+// GB300 against two CTAs of two buffers and one CTA of four, it is the shape
+// whose whole steps match the plain-load kernel (N = 2^24 and 1.2e8 at P = 8,
+// 2^27 at P = 4).
 #ifndef ZG_TMA_CTAS_PER_SM
-#define ZG_TMA_CTAS_PER_SM 2
+#define ZG_TMA_CTAS_PER_SM 1
 #endif
 constexpr int kTmaCtasPerSm = ZG_TMA_CTAS_PER_SM;
 #ifndef ZG_TMA_MAX_STAGES
-#define ZG_TMA_MAX_STAGES 4
+#define ZG_TMA_MAX_STAGES 3
 #endif
 static_assert(ZG_TMA_MAX_STAGES >= 2 && ZG_TMA_MAX_STAGES <= 8, "the kernel holds eight barriers");
 
@@ -21,8 +25,8 @@ cudaError_t launch_step_tma(int p, const uint16_t *const *g, int64_t n, float in
         for (int r = 0; r < P; ++r) src.g[r] = g[r];
         const tma::Layout lay = tma::Layout::of(P);
         // Ring buffers per CTA: as many (2..ZG_TMA_MAX_STAGES) as fit when kTmaCtasPerSm CTAs
-        // share an SM's 228 KB, so that more warps hide each tile's compute;
-        // if two buffers do not fit that way (large P), one CTA per SM.
+        // share an SM's 228 KB; if two buffers do not fit that way, one CTA
+        // per SM with as many as fit (two at P = 16).
         const int sm_bytes = 227 * 1024 - 1024;
         int stages = sm_bytes / kTmaCtasPerSm / int(lay.stage_bytes);
         if (stages < 2) stages = sm_bytes / int(lay.stage_bytes);
@@ -34,9 +38,9 @@ cudaError_t launch_step_tma(int p, const uint16_t *const *g, int64_t n, float in
         if (e != cudaSuccess) return e;
         const int64_t covered = (n / kVec) * kVec;
         const int64_t tiles = (covered + tma::kTile - 1) / tma::kTile;
-        const int wave = wave_blocks(reinterpret_cast<const void *>(fn), tma::kThreads, smem);
+        const int wave = wave_blocks(reinterpret_cast<const void *>(fn), tma::kWsThreads, smem);
         const int blocks = int(tiles < 1 ? 1 : (tiles < wave ? tiles : wave));
-        return launch_dependent(fn, blocks, tma::kThreads, smem, st, src, n, inv, k, state, sc, stages, wait_limit);
+        return launch_dependent(fn, blocks, tma::kWsThreads, smem, st, src, n, inv, k, state, sc, stages, wait_limit);
     });
 }
 
