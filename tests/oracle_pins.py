@@ -15,6 +15,7 @@ What pins what:
   - two-step closed form with two different gradients, written out;
   - the clip + AdamW chain against torch.nn.utils.clip_grad_norm_ and
     torch.optim.AdamW (another rounding order, so to rounding);
+  - the parameters after a step are the torch bf16 cast of the new weights;
   - clip: a vector of one repeated value has norm |a| sqrt(N);
   - norm: index-order binary64 sum vs math.fsum (correctly rounded);
   - averaging and loss scale on integer-valued gradients (exact);
@@ -188,6 +189,32 @@ def pin_adamw_and_clip_vs_torch(lib):
         diff = np.abs(mine.astype(np.float64) - theirs)
         assert diff.max() <= 2e-5 * np.sqrt(np.mean(theirs * theirs)), diff.max()
         assert np.median(diff / np.maximum(np.abs(theirs), 1e-30)) <= 2e-6
+
+
+def pin_params_are_bf16_of_new_weights(lib):
+    """The all-gathered parameters are the updated master weights rounded to
+    bf16 (Zero From Scratch, item 7: the all-gather hands every rank the
+    updated parameters; the pages' mixed precision keeps them in bf16): after
+    every applied step p equals PyTorch's round-to-nearest-even cast of the new
+    w, bit for bit, and a skipped step leaves p as it was."""
+    import torch
+
+    rng = np.random.default_rng(23)
+    n, p = 2048, 3
+    w0 = (rng.standard_normal(n) * 0.02).astype(np.float32)
+    ref = _opt(lib, w0)
+    for t in range(4):
+        grads = [_trunc(rng.standard_normal(n).astype(np.float32) * np.float32(1e-3 * 1024)) for _ in range(p)]
+        if t == 2:
+            grads[1][5] = 0x7F80  # +inf: this step is skipped
+        before = ref.p.copy()
+        dec = ref.step(grads, 1024.0)
+        if dec.found_inf:
+            assert ref.p.tobytes() == before.tobytes()
+        else:
+            want = torch.from_numpy(ref.w.copy()).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+            assert ref.p.tobytes() == want.tobytes()
+            assert ref.p.tobytes() != before.tobytes()
 
 
 def pin_clip_constant_vector(lib):
@@ -632,6 +659,7 @@ PINS = [
     pin_constant_gradient,
     pin_two_step_closed_form,
     pin_adamw_and_clip_vs_torch,
+    pin_params_are_bf16_of_new_weights,
     pin_clip_constant_vector,
     pin_norm_vs_fsum,
     pin_average_and_unscale,

@@ -57,6 +57,15 @@ MUTANTS = {
     "gather_mx_scale_per_64": ("scales[r][k / 32]", "scales[r][k / 64]"),
     "gather_mx_truncates": ("out[i - lo] = orc_f32_to_bf16(orc_mx_decode(codes[r][k], scales[r][k / 32]));",
                             "out[i - lo] = (uint16_t)(bits_from_f32(orc_mx_decode(codes[r][k], scales[r][k / 32])) >> 16);"),
+    "norm_eps_dropped": ("double q = hp->max_grad_norm / (d->norm + hp->norm_eps);",
+                         "double q = hp->max_grad_norm / d->norm;"),
+    "decay_after_update": ("        float wi = w[i] - lrwd * w[i];\n        wi = wi - lr * (mh / den);",
+                           "        float wi = w[i] - lr * (mh / den);\n        wi = wi - lrwd * wi;"),
+    "second_moment_mixes_clip": ("float vi = b2 * v[i] + omb2 * (ga * ga);", "float vi = b2 * v[i] + omb2 * (ga * g[i]);"),
+    "powers_in_binary32": ("    d->b1p = now->b1p * hp->beta1;\n    d->b2p = now->b2p * hp->beta2;",
+                           "    d->b1p = (float)(now->b1p * hp->beta1);\n    d->b2p = (float)(now->b2p * hp->beta2);"),
+    "params_from_old_weights": ("        w[i] = wi;\n        p[i] = orc_f32_to_bf16(wi);",
+                                "        p[i] = orc_f32_to_bf16(w[i]);\n        w[i] = wi;"),
     "running_power_reset": ("    ctr->b1p = 1.0;\n    ctr->b2p = 1.0;\n    for (int64_t k = 0; k < t; ++k) {",
                             "    ctr->b1p = 1.0;\n    ctr->b2p = 1.0;\n    for (int64_t k = 1; k < t; ++k) {"),
 }
