@@ -233,6 +233,15 @@ def pin_clip_constant_vector(lib):
     assert opt2.step([g], 1.0).clip == 1.0
     # the clipped gradient has norm max_norm * norm / (norm + 1e-6)
     assert abs(8.0 * d.clip - 8.0 / (8.0 + 1e-6)) <= 8.0 * _ulp(want)
+    # the factor is the ratio taken in binary64 and rounded once to binary32:
+    # for constant vectors the norm is exactly |a| * 64 (a^2 and the sum of
+    # 4096 of them are exact), so the factor is known exactly for every a
+    rng = np.random.default_rng(29)
+    for a in _trunc(rng.uniform(0.02, 10.0, 24).astype(np.float32) * rng.choice([-1, 1], 24).astype(np.float32)):
+        av = float((np.uint32(a) << np.uint32(16)).view(np.float32))
+        d = _opt(lib, np.zeros(n), weight_decay=0.0, max_grad_norm=1.0).step([np.full(n, a, np.uint16)], 1.0)
+        assert d.norm == abs(av) * 64.0
+        assert d.clip == float(np.float32(1.0 / (abs(av) * 64.0 + 1e-6))), (av, d.clip)
 
 
 def pin_norm_vs_fsum(lib):

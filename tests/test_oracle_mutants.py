@@ -2,12 +2,14 @@
 that the pins catch it: a dropped term, a wrong sign, index or constant, a
 swapped operand, a wrong rounding tie rule. The real oracle source is never
 modified; each mutant is compiled from a temporary copy and its pins run in a
-child process, so a mutant that crashes cannot take the test run down.
+child process of its own (several at a time), so a mutant that crashes cannot
+take the test run down.
 """
 import json
 import os
 import subprocess
 import sys
+from concurrent.futures import ThreadPoolExecutor
 
 import pytest
 
@@ -66,6 +68,15 @@ MUTANTS = {
                            "    d->b1p = (float)(now->b1p * hp->beta1);\n    d->b2p = (float)(now->b2p * hp->beta2);"),
     "params_from_old_weights": ("        w[i] = wi;\n        p[i] = orc_f32_to_bf16(wi);",
                                 "        p[i] = orc_f32_to_bf16(w[i]);\n        w[i] = wi;"),
+    "unscale_before_sum": ("        for (int r = 0; r < p; ++r)\n            s = s + orc_bf16_to_f32(grads[r][i]);\n        g[i - lo] = s * inv;",
+                           "        for (int r = 0; r < p; ++r)\n            s = s + orc_bf16_to_f32(grads[r][i]) * inv;\n        g[i - lo] = s;"),
+    "mx_amax_signed": ("        else if (fabs(vals[j]) > amax)\n            amax = fabs(vals[j]);",
+                       "        else if (vals[j] > amax)\n            amax = vals[j];"),
+    "mx_zero_block_scale_one": ("    if (amax == 0.0) {\n        e = -127;", "    if (amax == 0.0) {\n        e = 0;"),
+    "clip_in_binary32": ("        double q = hp->max_grad_norm / (d->norm + hp->norm_eps);",
+                         "        double q = (float)hp->max_grad_norm / ((float)d->norm + (float)hp->norm_eps);"),
+    "mx_nan_scale_ignored": ("    if (scale == 0xff)\n        return NAN;\n", ""),
+    "bias_correction_binary32_subtract": ("    d->bc1 = (float)(1.0 - d->b1p);", "    d->bc1 = 1.0f - (float)d->b1p;"),
     "running_power_reset": ("    ctr->b1p = 1.0;\n    ctr->b2p = 1.0;\n    for (int64_t k = 0; k < t; ++k) {",
                             "    ctr->b1p = 1.0;\n    ctr->b2p = 1.0;\n    for (int64_t k = 1; k < t; ++k) {"),
 }
@@ -79,14 +90,18 @@ print("FAILED=" + json.dumps(oracle_pins.run_all(lib)))
 """
 
 
-@pytest.mark.parametrize("name", sorted(MUTANTS))
-def test_mutant_is_caught(name, tmp_path):
+def _run_mutant(name: str, workdir: str) -> tuple[str, int, list | None]:
+    """Compile one mutant in its own folder and run every pin on it in a child
+    process; returns (name, the child's exit status, the failed pins)."""
     find, repl = MUTANTS[name]
     src = open(SRC).read()
-    assert src.count(find) == 1, f"mutation site for {name} not found exactly once"
-    mutant_src = tmp_path / "mutant.c"
-    mutant_src.write_text(src.replace(find, repl))
-    lib = oracle.build(str(mutant_src), str(tmp_path / "libmutant.so"))
+    if src.count(find) != 1:
+        return name, -1, None
+    os.makedirs(workdir, exist_ok=True)
+    mutant_src = os.path.join(workdir, "mutant.c")
+    with open(mutant_src, "w") as f:
+        f.write(src.replace(find, repl))
+    lib = oracle.build(mutant_src, os.path.join(workdir, "libmutant.so"))
     root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
     code = _CHILD.format(root=root, tests=os.path.join(root, "tests"), lib=lib)
     proc = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=300)
@@ -94,6 +109,23 @@ def test_mutant_is_caught(name, tmp_path):
     for line in proc.stdout.splitlines():
         if line.startswith("FAILED="):
             failed = json.loads(line[len("FAILED="):])
+    return name, proc.returncode, failed
+
+
+@pytest.fixture(scope="module")
+def outcomes(tmp_path_factory):
+    """Every mutant built and run once, several child processes at a time
+    (each still alone in its process, so a crash stays contained)."""
+    base = tmp_path_factory.mktemp("mutants")
+    workers = max(1, min(8, os.cpu_count() or 1))
+    with ThreadPoolExecutor(workers) as ex:
+        runs = ex.map(lambda n: _run_mutant(n, str(base / n)), sorted(MUTANTS))
+        return {name: (rc, failed) for name, rc, failed in runs}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name, outcomes):
+    rc, failed = outcomes[name]
+    assert not (rc == -1 and failed is None), f"mutation site for {name} not found exactly once"
     # a crash of the child also counts as caught; a clean run with no failed pin does not
-    assert proc.returncode != 0 or (failed is not None and len(failed) > 0), \
-        f"mutant {name} passed every pin"
+    assert rc != 0 or (failed is not None and len(failed) > 0), f"mutant {name} passed every pin"
