@@ -325,6 +325,12 @@ def pin_bf16_rounding_vs_torch(lib):
     want = torch.from_numpy(x.copy()).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
     got = oracle.f32_to_bf16(x, lib=lib)
     assert np.array_equal(got, want)
+    # NaN stays NaN (torch returns one canonical NaN, so only NaN-ness is
+    # compared; the values reach the oracle as Python floats, already quiet)
+    nan_bits = np.array([0x7F800001, 0x7F808000, 0x7FC00000, 0xFF800001, 0x7FFFFFFF, 0xFFBFFFFF], np.uint32)
+    got_nan = oracle.f32_to_bf16(nan_bits.view(np.float32), lib=lib).astype(np.uint32) << np.uint32(16)
+    assert np.all(np.isnan(got_nan.view(np.float32)))
+    assert np.all(np.isnan(torch.from_numpy(nan_bits.view(np.float32).copy()).to(torch.bfloat16).float().numpy()))
 
 
 def pin_e4m3_values_vs_torch(lib):

@@ -77,6 +77,7 @@ MUTANTS = {
                          "        double q = (float)hp->max_grad_norm / ((float)d->norm + (float)hp->norm_eps);"),
     "mx_nan_scale_ignored": ("    if (scale == 0xff)\n        return NAN;\n", ""),
     "bias_correction_binary32_subtract": ("    d->bc1 = (float)(1.0 - d->b1p);", "    d->bc1 = 1.0f - (float)d->b1p;"),
+    "found_inf_only_inf": ("    d->found_inf = !isfinite(sumsq);", "    d->found_inf = isinf(sumsq);"),
     "running_power_reset": ("    ctr->b1p = 1.0;\n    ctr->b2p = 1.0;\n    for (int64_t k = 0; k < t; ++k) {",
                             "    ctr->b1p = 1.0;\n    ctr->b2p = 1.0;\n    for (int64_t k = 1; k < t; ++k) {"),
 }
