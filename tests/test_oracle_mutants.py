@@ -78,6 +78,9 @@ MUTANTS = {
     "mx_nan_scale_ignored": ("    if (scale == 0xff)\n        return NAN;\n", ""),
     "bias_correction_binary32_subtract": ("    d->bc1 = (float)(1.0 - d->b1p);", "    d->bc1 = 1.0f - (float)d->b1p;"),
     "found_inf_only_inf": ("    d->found_inf = !isfinite(sumsq);", "    d->found_inf = isinf(sumsq);"),
+    "sharded_norm_drops_last_rank": ("    for (int r = 0; r < p; ++r)\n        ss = ss + partial[r];",
+                                     "    for (int r = 0; r < p - 1; ++r)\n        ss = ss + partial[r];"),
+    "sharded_norm_is_a_local_norm": ("    for (int r = 0; r < p; ++r)\n        ss = ss + partial[r];", "    ss = partial[0];"),
     "running_power_reset": ("    ctr->b1p = 1.0;\n    ctr->b2p = 1.0;\n    for (int64_t k = 0; k < t; ++k) {",
                             "    ctr->b1p = 1.0;\n    ctr->b2p = 1.0;\n    for (int64_t k = 1; k < t; ++k) {"),
 }
