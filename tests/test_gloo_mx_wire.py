@@ -1,5 +1,5 @@
 """The stage-two exchange with the MXFP8 wire, on CPU (gloo), world sizes 2
-and 3.
+to 4.
 
 Zero From Scratch, item 14: MXFP8 halves the gradient bytes on the wire.
 Each process encodes its own rank's bf16 gradient (E4M3 codes, one E8M0 scale
@@ -100,7 +100,7 @@ def _worker(rank: int, world: int, port: int, out_dir: str) -> None:
         dist.destroy_process_group()
 
 
-@pytest.mark.parametrize("world", [2, 3])
+@pytest.mark.parametrize("world", [2, 3, 4])
 def test_mx_wire_exchange_over_gloo_matches_single_process(world, tmp_path):
     mp.start_processes(_worker, args=(world, _free_port(), str(tmp_path)), nprocs=world, start_method="spawn")
     w, steps = _inputs(world)

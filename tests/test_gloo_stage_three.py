@@ -1,5 +1,5 @@
 """The stage-three exchange with real collectives, on CPU (gloo), world sizes 2
-and 3.
+to 4.
 
 DeepSpeed documentation review, paragraph on the three stages: stage three
 splits the parameters as well, and each layer collects its parameters from
@@ -127,7 +127,7 @@ def _worker(rank: int, world: int, port: int, out_dir: str) -> None:
         dist.destroy_process_group()
 
 
-@pytest.mark.parametrize("world", [2, 3])
+@pytest.mark.parametrize("world", [2, 3, 4])
 def test_stage_three_over_gloo_matches_single_process(world, tmp_path):
     mp.start_processes(_worker, args=(world, _free_port(), str(tmp_path)), nprocs=world, start_method="spawn")
     w, steps = _inputs(world)
