@@ -956,12 +956,13 @@ cudaError_t with_ranks(int p, F &&f)
 
 // ------------------------------------------------------------------ TMA-staged step pass
 //
-// The same fused step, with the operands of each 2048-element tile staged
+// The same fused step, with the operands of each tile (4096 elements up to
+// P = 4, 2048 from P = 5) staged
 // in shared memory by 1-D bulk asynchronous copies (cp.async.bulk, global to
 // this CTA's shared memory, completion counted in bytes on an mbarrier): P
 // bf16 gradient slices and the fp32 w, m, v. The CTA is warp-specialised:
 // one producer warp walks the CTA's tiles through a ring of `stages`
-// buffers, and eight consumer warps (8 elements per thread per tile) read a
+// buffers, and the consumer warps (8 elements per thread per tile) read a
 // buffer into registers, release it and compute. Each buffer has a "full"
 // barrier (the producer's expect_tx arrival plus the copied bytes) and an
 // "empty" barrier (one arrival per consumer warp), so no block-wide barrier
@@ -977,14 +978,19 @@ cudaError_t with_ranks(int p, F &&f)
 namespace zg {
 namespace tma {
 
-#ifndef ZG_TMA_TILE
-#define ZG_TMA_TILE 2048
-#endif
-constexpr int kTile = ZG_TMA_TILE;    // elements per tile
+// Elements per tile, by rank count: up to P = 4 a tile holds few gradient
+// bytes, so tiles are 4096 elements (sixteen consumer warps, two buffers);
+// from P = 5 on, 2048 elements (eight consumer warps, three buffers; two at
+// P = 16). Measured on GB300, each choice is the faster one where it is used.
+constexpr int kTileSmallP = 4096;
+constexpr int kTileLargeP = 2048;
+template <int P>
+struct TileFor {
+    static constexpr int value = P <= 4 ? kTileSmallP : kTileLargeP;
+};
 #ifndef ZG_TMA_REVERSE
 #define ZG_TMA_REVERSE ZG_STEP_REVERSE
 #endif
-constexpr int kThreads = kTile / kVec;  // 8 elements per thread
 constexpr long long kDrainLimit = 1LL << 22;
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p)
@@ -1043,18 +1049,19 @@ struct Layout {
     int p;
     uint32_t grad_bytes;   // per rank per full tile
     uint32_t stage_bytes;  // P gradient slices + w, m, v
-    __host__ __device__ static Layout of(int p)
+    __host__ __device__ static Layout of(int p, int tile)
     {
         Layout l;
         l.p = p;
-        l.grad_bytes = kTile * 2;
-        l.stage_bytes = p * l.grad_bytes + 3 * kTile * 4;
+        l.grad_bytes = uint32_t(tile) * 2;
+        l.stage_bytes = p * l.grad_bytes + 3 * uint32_t(tile) * 4;
         return l;
     }
 };
 
-constexpr int kConsumers = kThreads;        // 8 elements per consumer thread per tile
-constexpr int kWsThreads = kConsumers + 32;  // plus the producer warp
+// Threads of a CTA for a tile size: one consumer thread per 8 elements, plus
+// the producer warp.
+constexpr int ws_threads(int tile) { return tile / kVec + 32; }
 #ifndef ZG_TMA_WS_MINB
 #define ZG_TMA_WS_MINB 1
 #endif
@@ -1076,8 +1083,8 @@ __device__ __forceinline__ bool mbar_wait_or_abort(uint64_t *bar, uint32_t parit
     return false;
 }
 
-template <int P>
-__global__ void __launch_bounds__(kWsThreads, ZG_TMA_WS_MINB)
+template <int P, int TILE>
+__global__ void __launch_bounds__(ws_threads(TILE), ZG_TMA_WS_MINB)
     step_kernel_tma(Bf16Src<P> src, int64_t n, float inv, StepK k, State st, Scalars *sc, int stages,
                     long long wait_limit)
 {
@@ -1091,7 +1098,9 @@ __global__ void __launch_bounds__(kWsThreads, ZG_TMA_WS_MINB)
     pdl_trigger();
     float c, bc1, bc2;
     int skip = step_prologue(sc, c, bc1, bc2);
-    const Layout lay = Layout::of(P);
+    constexpr int kTile = TILE;
+    constexpr int kConsumers = TILE / kVec;  // 8 elements per consumer thread per tile
+    const Layout lay = Layout::of(P, TILE);
     const int64_t nvec = n / kVec;
     const int64_t covered = nvec * kVec;  // elements the tiles cover; the rest is the scalar tail
     const int64_t ntiles = (covered + kTile - 1) / kTile;

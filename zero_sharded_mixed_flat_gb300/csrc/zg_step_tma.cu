@@ -3,10 +3,10 @@
 
 namespace zg {
 
-// One warp-specialised CTA per SM with three ring buffers: measured on
-// GB300 against two CTAs of two buffers and one CTA of four, it is the shape
-// whose whole steps match the plain-load kernel (N = 2^24 and 1.2e8 at P = 8,
-// 2^27 at P = 4).
+// One warp-specialised CTA per SM. With 2048-element tiles (P >= 5) three
+// ring buffers: measured on GB300 against two CTAs of two buffers and one CTA
+// of four, the shape whose whole steps match or beat the plain-load kernel;
+// with 4096-element tiles (P <= 4) two buffers.
 #ifndef ZG_TMA_CTAS_PER_SM
 #define ZG_TMA_CTAS_PER_SM 1
 #endif
@@ -23,24 +23,27 @@ cudaError_t launch_step_tma(int p, const uint16_t *const *g, int64_t n, float in
         constexpr int P = decltype(rk)::value;
         Bf16Src<P> src;
         for (int r = 0; r < P; ++r) src.g[r] = g[r];
-        const tma::Layout lay = tma::Layout::of(P);
+        constexpr int T = tma::TileFor<P>::value;
+        constexpr int threads = tma::ws_threads(T);
+        const tma::Layout lay = tma::Layout::of(P, T);
+        const int cap = T == tma::kTileSmallP ? 2 : ZG_TMA_MAX_STAGES;
         // Ring buffers per CTA: as many (2..ZG_TMA_MAX_STAGES) as fit when kTmaCtasPerSm CTAs
         // share an SM's 228 KB; if two buffers do not fit that way, one CTA
         // per SM with as many as fit (two at P = 16).
         const int sm_bytes = 227 * 1024 - 1024;
         int stages = sm_bytes / kTmaCtasPerSm / int(lay.stage_bytes);
         if (stages < 2) stages = sm_bytes / int(lay.stage_bytes);
-        stages = stages > ZG_TMA_MAX_STAGES ? ZG_TMA_MAX_STAGES : stages;
+        stages = stages > cap ? cap : stages;
         if (stages < 2) return cudaErrorInvalidConfiguration;
         const size_t smem = size_t(stages) * lay.stage_bytes;
-        auto *fn = &tma::step_kernel_tma<P>;
+        auto *fn = &tma::step_kernel_tma<P, T>;
         cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
         if (e != cudaSuccess) return e;
         const int64_t covered = (n / kVec) * kVec;
-        const int64_t tiles = (covered + tma::kTile - 1) / tma::kTile;
-        const int wave = wave_blocks(reinterpret_cast<const void *>(fn), tma::kWsThreads, smem);
+        const int64_t tiles = (covered + T - 1) / T;
+        const int wave = wave_blocks(reinterpret_cast<const void *>(fn), threads, smem);
         const int blocks = int(tiles < 1 ? 1 : (tiles < wave ? tiles : wave));
-        return launch_dependent(fn, blocks, tma::kWsThreads, smem, st, src, n, inv, k, state, sc, stages, wait_limit);
+        return launch_dependent(fn, blocks, threads, smem, st, src, n, inv, k, state, sc, stages, wait_limit);
     });
 }
 
