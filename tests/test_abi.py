@@ -96,3 +96,34 @@ def test_binding_refuses_host_tensors_before_any_call():
     with pytest.raises(TypeError, match="w must be a CUDA tensor or pinned host memory"):
         zb.zg_bind(ctx, torch.zeros(64), torch.zeros(64), torch.zeros(64), host_bf16)
 
+
+
+def _header_prototypes() -> dict[str, tuple[str, int]]:
+    """name -> (return type, parameter count) for every function in zg.h."""
+    text = open(os.path.join(ROOT, "include", "zg.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = "\n".join(line for line in text.splitlines() if not line.lstrip().startswith("#"))
+    out = {}
+    for ret, name, params in re.findall(r"([A-Za-z_][\w\s\*]*?)\b(zg_[a-z0-9_]+)\s*\(([^)]*)\)\s*;", text):
+        params = params.strip()
+        count = 0 if params in ("", "void") else params.count(",") + 1
+        out[name] = (" ".join(ret.split()), count)
+    return out
+
+
+def test_binding_signatures_match_the_header(lib):
+    """Every function the binding declares has the header's parameter count and
+    a matching kind of return value, so the two cannot drift apart."""
+    protos = _header_prototypes()
+    assert set(protos) == set(declared_functions())
+    for name, (ret, count) in protos.items():
+        fn = getattr(lib, name)
+        assert len(fn.argtypes) == count, (name, len(fn.argtypes), count)
+        if ret == "void":
+            assert fn.restype is None, name
+        elif ret.endswith("*"):
+            assert fn.restype is ctypes.c_char_p, name  # the two string getters
+        elif ret == "int64_t":
+            assert fn.restype is ctypes.c_int64, name
+        else:
+            assert ret == "int" and fn.restype is ctypes.c_int, (name, ret)
