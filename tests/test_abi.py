@@ -127,3 +127,33 @@ def test_binding_signatures_match_the_header(lib):
             assert fn.restype is ctypes.c_int64, name
         else:
             assert ret == "int" and fn.restype is ctypes.c_int, (name, ret)
+
+
+def test_struct_layouts_match_the_header(tmp_path):
+    """zg_hparams and zg_step_info as the binding lays them out (ctypes) equal
+    what a C compiler makes of include/zg.h: size and every field's offset."""
+    import shutil
+    import subprocess
+
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    structs = {"zg_hparams": zb._Hp, "zg_step_info": zb._Info}
+    lines = ['#include <stddef.h>', '#include <stdio.h>', '#include "zg.h"', "int main(void) {"]
+    for cname, cls in structs.items():
+        lines.append(f'printf("{cname} size %zu\\n", sizeof({cname}));')
+        for field, _ in cls._fields_:
+            lines.append(f'printf("{cname} {field} %zu\\n", offsetof({cname}, {field}));')
+    lines += ["return 0;", "}"]
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines) + "\n")
+    exe = tmp_path / "layout"
+    subprocess.run([cc, "-std=c11", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
+    got = {}
+    for line in subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.splitlines():
+        cname, field, value = line.split()
+        got[(cname, field)] = int(value)
+    for cname, cls in structs.items():
+        assert got[(cname, "size")] == ctypes.sizeof(cls), cname
+        for field, _ in cls._fields_:
+            assert got[(cname, field)] == getattr(cls, field).offset, (cname, field)
