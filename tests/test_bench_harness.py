@@ -4,7 +4,6 @@ import io
 import json
 import os
 import socket
-import sys
 from contextlib import redirect_stdout
 
 import torch.distributed as dist
