@@ -71,7 +71,8 @@ extern "C" {
 
 /* Ways to run a bf16 step; all compute identical results. */
 #define ZG_VARIANT_LDG 0    /* fused step with 128-bit vector loads straight from HBM (default) */
-#define ZG_VARIANT_TMA 1    /* fused step with its operands staged in shared memory by bulk async copies */
+#define ZG_VARIANT_TMA 1    /* fused step, operands staged in a shared-memory ring by bulk async copies
+                              (one producer warp, consumer warps; tile size chosen by P) */
 #define ZG_VARIANT_STAGED 2 /* the norm pass also stores the reduced fp32 gradient; the step reads it */
 
 typedef struct CUstream_st *zg_stream; /* same type as cudaStream_t */
