@@ -157,3 +157,28 @@ def test_struct_layouts_match_the_header(tmp_path):
         assert got[(cname, "size")] == ctypes.sizeof(cls), cname
         for field, _ in cls._fields_:
             assert got[(cname, field)] == getattr(cls, field).offset, (cname, field)
+
+
+def test_plain_c_program_compiles_and_links_against_the_abi(lib, tmp_path):
+    """tests/c_abi_caller.c (the C caller the GPU test runs) builds with gcc
+    against include/zg.h alone and links with libzg.so and the CUDA runtime:
+    the header is plain C11 and every symbol it uses resolves. It is not run
+    here (that needs a GPU)."""
+    import glob
+    import shutil
+    import subprocess
+
+    cc = shutil.which("gcc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    cuda = os.path.dirname(os.path.dirname(os.path.realpath(zbuild.nvcc())))
+    hits = [h for pat in ("lib64/libcudart.so", "targets/*/lib/libcudart.so", "lib/libcudart.so")
+            for h in glob.glob(os.path.join(cuda, pat))]
+    if not hits:
+        pytest.skip("no CUDA runtime library to link against")
+    pkg = os.path.dirname(zb.LIB_PATH)
+    subprocess.run([cc, "-std=c11", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"),
+                    "-I", os.path.join(cuda, "include"), os.path.join(ROOT, "tests", "c_abi_caller.c"),
+                    "-o", str(tmp_path / "caller"), "-L", pkg, "-lzg", "-L", os.path.dirname(hits[0]), "-lcudart",
+                    f"-Wl,-rpath,{pkg}"], check=True)
+    assert (tmp_path / "caller").exists()
