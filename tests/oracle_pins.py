@@ -23,6 +23,7 @@ What pins what:
   - bf16 rounding vs the torch cast; E4M3 values vs torch's float8_e4m3fn;
     the encoder vs a nearest-value table search with ties to even;
   - the MX scale rule on blocks built by hand from the format;
+  - the MX round trip within half an E4M3 spacing at the block's scale;
   - shard layout invariants; identical learning (sharded == unsharded);
   - resume (set_step) reproduces an uninterrupted run;
   - power-of-two loss-scale invariance of the whole step;
@@ -433,6 +434,39 @@ def pin_mx_scale_rule(lib):
     assert oracle.mx_decode(0x7E, 246, lib=lib) == 448.0 * 2.0 ** 119
 
 
+def pin_mx_roundtrip_error_bound(lib):
+    """Decoding an encoded block returns every value to within half an E4M3
+    spacing at the block's scale (spacing 2^(floor(log2 |y|) - 3) for normal
+    magnitudes, 2^-9 below 2^-6, where y = x 2^-e), or saturates exactly to
+    448 2^e; the scale follows the block's largest magnitude (e = floor(log2
+    amax) - 8). Random blocks over sixty binades, signs mixed, zeros
+    included: a bound from the format definition, not a second encoder."""
+    rng = np.random.default_rng(37)
+    nblk = 400
+    mag = np.exp2(rng.uniform(-30, 30, nblk))[:, None] * np.exp2(rng.uniform(-12, 0, (nblk, 32)))
+    x = (mag * rng.choice([-1.0, 1.0], (nblk, 32))).astype(np.float32)
+    x[rng.random((nblk, 32)) < 0.05] = 0.0
+    xb = _trunc(x.ravel())
+    xv = (xb.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64).reshape(nblk, 32)
+    codes, scales = oracle.mx_encode(xb, lib=lib)
+    for b in range(nblk):
+        amax = np.max(np.abs(xv[b]))
+        e = int(scales[b]) - 127
+        if amax == 0.0:
+            assert scales[b] == 0
+            continue
+        assert e == max(-127, min(127, math.floor(math.log2(amax)) - 8)), (b, e, amax)
+        for j in range(32):
+            y = xv[b, j] * 2.0 ** -e
+            d = oracle.mx_decode(int(codes[32 * b + j]), int(scales[b]), lib=lib) * 2.0 ** -e
+            assert not math.isnan(d)
+            if abs(y) > 448.0:
+                assert d == math.copysign(448.0, y), (b, j, y, d)
+            else:
+                spacing = 2.0 ** (math.floor(math.log2(abs(y))) - 3) if abs(y) >= 2.0 ** -6 else 2.0 ** -9
+                assert abs(d - y) <= spacing / 2, (b, j, y, d)
+
+
 def pin_mx_loss_scale_shifts_scale_only(lib):
     import zero_sharded_mixed_flat_gb300.synth as synth
 
@@ -685,6 +719,7 @@ PINS = [
     pin_e4m3_encoder_exhaustive,
     pin_mx_scale_rule,
     pin_mx_loss_scale_shifts_scale_only,
+    pin_mx_roundtrip_error_bound,
     pin_mx_f32_encoder,
     pin_shard_layout,
     pin_identical_learning,
