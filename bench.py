@@ -1,24 +1,31 @@
 """Benchmark: the sharded mixed-precision optimizer step on one GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload flat16m_p8] [--variant ldg|tma]
+                    [--workload flat3b_p8] [--variant ldg|tma|staged]
 
 A step is one whole optimizer step of the library on one batch of resident
-synthetic inputs: the norm pass (reduce-scatter + unscale + global norm +
+synthetic gradients: the norm pass (reduce-scatter + unscale + global norm +
 found-inf + clip decision) and the fused shard step (reduce-scatter +
 unscale + clip + AdamW on fp32 w/m/v + bf16 all-gather) over all P
-simulated ranks. Default workload: N = 2^24 parameters, P = 8 ranks, bf16
-gradients N(0, 1e-3) x 1024, AdamW lr 1e-3, betas 0.9/0.999, eps 1e-8,
-wd 0.01, clip 1.0. The working set (0.47 GB) exceeds the 129 MB L2, so no
-flush is needed between steps.
+simulated ranks. Default workload: the largest that fits one GPU, N = 3e9
+parameters over P = 8 ranks (fp32 w, m, v: 36 GB; bf16 params: 6 GB; two
+batches of eight bf16 gradient buffers: 96 GB), gradients N(0, 1e-3) x 1024,
+AdamW lr 1e-3, betas 0.9/0.999, eps 1e-8, wd 0.01, clip 1.0. Two gradient
+batches (the workload's steps 1 and 2) alternate, so every step reads fresh
+gradients; the working set is far larger than the 129 MB L2, so no flush is
+needed between steps.
 
 Prints one JSON line (rank 0). ``value`` is parameters updated per second
-over the whole job; ``roofline`` describes the fused shard-step kernel
-against the measured HBM bandwidth; ``e2e`` is the same metric through the
-C ABI with the gradients copied from pinned host memory every step and the
-step scalars read back every step (step k+1's copy overlapped with step k
-through two device input slots; ``e2e.serial`` without that overlap);
-``cpu_baseline`` is the oracle timed on the host.
+over the whole job; ``kernels`` gives every pass's mean and spread over at
+least 20 launches, each between its own CUDA events, and its bandwidth on
+the algorithmic bytes and on the DRAM bytes ncu measured; ``roofline``
+describes the fused shard-step pass against the measured HBM bandwidth;
+``e2e`` is the same metric through the C ABI with the gradients copied from
+pinned host memory every step and the step scalars read back every step
+(step k+1's copy overlapped with step k through two device input slots;
+``e2e.serial`` without that overlap); ``configs`` repeats the measurement on
+the 2^24-parameter, GPT-2-small and MXFP8 workloads, each in its own short
+loop; ``cpu_baseline`` is the oracle timed on the host.
 
 Under torchrun (N > 1) every GPU runs its own independent P-rank problem (no
 collective on the data path: the simulated ranks live inside one GPU), so
@@ -48,6 +55,7 @@ METRIC = "optimizer-step params/sec"
 UNIT = "params/s"
 FALLBACK_HBM_GBS = 6800.0
 SCALARS_D2H_BYTES = 112  # sizeof the device scalar block zg_get_info copies back
+COPY_PIECE = 1 << 30     # bytes per host-to-device copy in the end-to-end leg
 
 
 # --------------------------------------------------------------------- clocks
@@ -527,21 +535,222 @@ def time_stage3(opt, wl, K: int, peak: float, tokens: int = 8192) -> dict:
                 (accounting.MX_BYTES_PER_ELEMENT if mx else accounting.PARAM_BF16) * wl.n, wl.p, "all_gather")}
 
 
+# --------------------------------------------------------------------- inputs and steps
+
+# The workloads timed beside the headline one, each in its own short loop.
+CONFIG_WORKLOADS = ("flat16m_p8", "gpt2small_p8", "mxfp8_128m_p8")
+CONFIG_STEPS = {"flat16m_p8": 200, "gpt2small_p8": 40, "mxfp8_128m_p8": 40}
+MIN_PASS_SAMPLES = 20
+
+
+def host_mem_available() -> float:
+    """Bytes of host memory the kernel reports as available (inf if unknown)."""
+    try:
+        with open("/proc/meminfo") as f:
+            for line in f:
+                if line.startswith("MemAvailable:"):
+                    return int(line.split()[1]) * 1024.0
+    except OSError:
+        pass
+    return float("inf")
+
+
+def load_batches(wl, nbatch: int, keep_host: bool):
+    """``nbatch`` gradient batches of the workload (its steps 1, 2, ...), each
+    a device tensor [P, P*S] of bf16 whose row r is rank r's buffer, copied to
+    the device before anything is timed. With ``keep_host`` batch 0 is drawn
+    straight into pinned host memory, which is returned as well (the
+    end-to-end leg copies a step's inputs from it)."""
+    import numpy as np
+    import torch
+
+    from zero_sharded_mixed_flat_gb300 import synth
+
+    total = synth.padded_len(wl)
+    dev, host = [], None
+    for b in range(nbatch):
+        d = torch.empty((wl.p, total), dtype=torch.bfloat16, device="cuda")
+        if b == 0 and keep_host:
+            host = torch.empty((wl.p, total), dtype=torch.int16, pin_memory=True)
+            hn = host.numpy().view(np.uint16)
+            for r in range(wl.p):
+                synth.grads_bf16(wl, b + 1, r, 0, total, out=hn[r])
+            d.view(torch.int16).copy_(host)
+        else:
+            for r in range(wl.p):
+                h = synth.grads_bf16(wl, b + 1, r, 0, total)
+                d[r].view(torch.int16).copy_(torch.from_numpy(h.view(np.int16)))
+        dev.append(d)
+    torch.cuda.synchronize()
+    return dev, host
+
+
+class Stepper:
+    """Issues whole optimizer steps through the library, cycling over the
+    resident gradient batches (a fresh batch every step when there are two).
+    On the MX workload a step first encodes the P ranks' gradients (the
+    wire payload), then runs the MX norm and step passes."""
+
+    def __init__(self, opt, wl, dev, stream):
+        import torch
+
+        from zero_sharded_mixed_flat_gb300 import synth
+
+        self.opt, self.wl, self.stream = opt, wl, stream
+        self.rows = [list(d.unbind(0)) for d in dev]
+        self.k = 0
+        if wl.mx:
+            total = synth.padded_len(wl)
+            self.codes = [torch.empty(total, dtype=torch.uint8, device="cuda") for _ in range(wl.p)]
+            self.scales = [torch.empty(total // 32, dtype=torch.uint8, device="cuda") for _ in range(wl.p)]
+
+    def step(self, ev=None, stream=None):
+        """One whole step; with events, mark [start, after norm, after step,
+        after the encodes] (the last only on the MX workload)."""
+        from zero_sharded_mixed_flat_gb300 import binding as zb
+
+        st = stream if stream is not None else self.stream
+        g = self.rows[self.k % len(self.rows)]
+        self.k += 1
+        ls = self.wl.loss_scale
+        ctx = self.opt.ctx
+        if ev is None and not self.wl.mx:
+            zb.zg_step(ctx, g, ls, st)
+            return
+        if ev is not None:
+            ev[0].record(st)
+        if self.wl.mx:
+            for r in range(self.wl.p):
+                zb.zg_quant_mxfp8(g[r], self.codes[r], self.scales[r], self.wl.n, st)
+            if ev is not None:
+                ev[3].record(st)
+            zb.zg_grad_norm_mxfp8(ctx, self.codes, self.scales, ls, st)
+        else:
+            zb.zg_grad_norm(ctx, g, ls, st)
+        if ev is not None:
+            ev[1].record(st)
+        if self.wl.mx:
+            zb.zg_shard_step_mxfp8(ctx, self.codes, self.scales, ls, st)
+        else:
+            zb.zg_shard_step(ctx, g, ls, st)
+        if ev is not None:
+            ev[2].record(st)
+
+
+def time_loop(stepper, K: int, world: int, clocks=None) -> float:
+    """Seconds for K back-to-back steps issued as a caller issues them (no
+    event between the passes), bracketed by barrier + synchronize and timed
+    with CUDA events on the launching stream; the max over ranks."""
+    import torch
+
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    if clocks is not None:
+        clocks.region(True)
+    e0.record(stepper.stream)
+    for _ in range(K):
+        stepper.step()
+    e1.record(stepper.stream)
+    torch.cuda.synchronize()
+    if clocks is not None:
+        clocks.region(False)
+    barrier(world)
+    return max_over_ranks(e0.elapsed_time(e1) / 1e3, world)
+
+
+def time_passes(stepper, samples: int) -> dict:
+    """Per-pass durations (ms) of ``samples`` steps, each pass bracketed by its
+    own events. The events keep the step pass from starting while the norm
+    pass drains, so these are the passes' own times, without that overlap."""
+    import torch
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(samples)]
+    torch.cuda.synchronize()
+    for i in range(samples):
+        stepper.step(ev[i])
+    torch.cuda.synchronize()
+    n0 = 3 if stepper.wl.mx else 0
+    out = {"norm": [e[n0].elapsed_time(e[1]) for e in ev], "step": [e[1].elapsed_time(e[2]) for e in ev]}
+    if stepper.wl.mx:
+        out["encode"] = [e[0].elapsed_time(e[3]) for e in ev]
+    return out
+
+
+def pass_stats(ms: list[float], bytes_per_launch: float, peak: float, traffic: float | None) -> dict:
+    """Mean, median, spread of a pass's launch times, and its bandwidth on the
+    algorithmic bytes and (when the ncu counters match the sources) on the
+    DRAM bytes ncu measured for the same launch."""
+    xs = sorted(ms)
+    mean_s = statistics.fmean(xs) / 1e3
+    st = {"launches": len(xs), "mean_us": mean_s * 1e6, "median_us": statistics.median(xs) * 1e3,
+          "min_us": xs[0] * 1e3, "max_us": xs[-1] * 1e3,
+          "stdev_us": statistics.stdev(xs) * 1e3 if len(xs) > 1 else 0.0,
+          "algorithmic_bytes": bytes_per_launch, "gbs": bytes_per_launch / mean_s / 1e9,
+          "frac": bytes_per_launch / mean_s / 1e9 / peak, "dram_bytes": traffic}
+    if traffic:
+        st.update(dram_gbs=traffic / mean_s / 1e9, frac_dram=traffic / mean_s / 1e9 / peak)
+    return st
+
+
+def launch_bytes(wl, variant: str, params: str) -> tuple[float, float, float]:
+    """Algorithmic bytes of one step pass, one norm pass and the P encodes."""
+    from zero_sharded_mixed_flat_gb300 import accounting
+
+    n, p = wl.n, wl.p
+    if wl.mx and variant == "staged":
+        return (accounting.staged_shard_step_bytes_per_param() * n, accounting.mx_staged_grad_norm_bytes_per_param(p) * n,
+                accounting.mx_quant_bytes_per_param() * p * n)
+    if wl.mx:
+        return (accounting.mx_shard_step_bytes_per_param(p) * n, accounting.mx_grad_norm_bytes_per_param(p) * n,
+                accounting.mx_quant_bytes_per_param() * p * n)
+    if variant == "staged":
+        return accounting.staged_shard_step_bytes_per_param() * n, accounting.staged_grad_norm_bytes_per_param(p) * n, 0.0
+    if params == "mxfp8":
+        return accounting.mx_params_shard_step_bytes_per_param(p) * n, accounting.grad_norm_bytes_per_param(p) * n, 0.0
+    return accounting.shard_step_bytes_per_param(p) * n, accounting.grad_norm_bytes_per_param(p) * n, 0.0
+
+
+def kernel_names(wl, variant: str, params: str) -> tuple[str, str]:
+    """Names the ncu counters are recorded under: (step pass, norm pass)."""
+    step = ("zg_shard_step_mxfp8" if wl.mx else "zg_shard_step") + \
+        {"staged": "_staged", "tma": "" if wl.mx else "_tma"}.get(variant, "")
+    if params == "mxfp8":
+        step += "_mxparams"
+    norm = ("zg_grad_norm_mxfp8" if wl.mx else "zg_grad_norm") + ("_staged" if variant == "staged" else "")
+    return step, norm
+
+
+def kernel_block(passes: dict, wl, key: str, variant: str, params: str, peak: float) -> dict:
+    """Every pass's statistics with its bandwidth (see pass_stats)."""
+    b_step, b_norm, b_quant = launch_bytes(wl, variant, params)
+    k_step, k_norm = kernel_names(wl, variant, params)
+    out = {"step": pass_stats(passes["step"], b_step, peak, recorded_traffic(k_step, key)),
+           "norm": pass_stats(passes["norm"], b_norm, peak, recorded_traffic(k_norm, key))}
+    if "encode" in passes:
+        t = recorded_traffic("zg_quant_mxfp8", key)
+        out["encode"] = pass_stats(passes["encode"], b_quant, peak, t * wl.p if t else None)
+        out["encode"]["launches_per_sample"] = wl.p
+    return out
+
+
 # --------------------------------------------------------------------- CUDA graphs
 
-def time_graph(opt, dev, ls, K: int, per_graph: int = 10) -> dict:
+def time_graph(stepper, K: int, per_graph: int = 10) -> dict:
     """The same steps captured `per_graph` at a time into one CUDA graph and
     replayed: what launch overhead the eager loop still pays."""
     import torch
 
     side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(side):
-        opt.step(dev, ls, side)  # launch configurations cached before capture
+        stepper.step(stream=side)  # launch configurations cached before capture
     side.synchronize()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=side):
         for _ in range(per_graph):
-            opt.step(dev, ls)
+            stepper.step(stream=side)
     reps = max(1, K // per_graph)
     for _ in range(2):
         g.replay()
@@ -553,9 +762,9 @@ def time_graph(opt, dev, ls, K: int, per_graph: int = 10) -> dict:
     e1.record()
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / (reps * per_graph)
-    info = opt.info()
+    info = stepper.opt.info()
     assert info.status == 0 and not info.found_inf
-    return {"value": opt.n / (ms / 1e3), "unit": UNIT, "ms_per_step": ms, "steps_per_graph": per_graph,
+    return {"value": stepper.wl.n / (ms / 1e3), "unit": UNIT, "ms_per_step": ms, "steps_per_graph": per_graph,
             "steps": reps * per_graph}
 
 
@@ -575,17 +784,24 @@ def time_e2e(h_in, slot_inputs, step_on, opt, stream, steps: int, world: int) ->
     copied = [torch.cuda.Event(), torch.cuda.Event()]
     consumed = [torch.cuda.Event(), torch.cuda.Event()]
 
+    def copy_in(k):
+        # pieces of at most COPY_PIECE bytes: one very large host-to-device
+        # copy measured well below the link rate on GB300
+        for d, h in zip(slot_inputs(k), h_in):
+            dflat, hflat = d.reshape(-1), h.reshape(-1)
+            step = max(1, COPY_PIECE // hflat.element_size())
+            for i in range(0, hflat.numel(), step):
+                dflat[i:i + step].copy_(hflat[i:i + step], non_blocking=True)
+
     def feed(k):
         with torch.cuda.stream(copy_stream):
             copy_stream.wait_event(consumed[k])
-            for d, h in zip(slot_inputs(k), h_in):
-                d.copy_(h, non_blocking=True)
+            copy_in(k)
             copied[k].record(copy_stream)
 
     def serial(count):
         for _ in range(count):
-            for d, h in zip(slot_inputs(0), h_in):
-                d.copy_(h, non_blocking=True)
+            copy_in(0)
             step_on(0)
             opt.info(stream)  # device->host read of the step result; synchronises
 
@@ -620,208 +836,242 @@ def time_e2e(h_in, slot_inputs, step_on, opt, stream, steps: int, world: int) ->
             "pipeline": "two device input slots; step k+1's inputs copied on a second stream during step k"}
 
 
-# --------------------------------------------------------------------- our arm
-
-def time_variant(name: str, wl, dev, stream, warmup: int, K: int, world: int) -> dict:
-    """The same device-resident steps with another bf16 variant of the library
-    (identical results): whole-step params/s and the step pass's bandwidth."""
+def e2e_leg(stepper, dev, host, args, world) -> dict:
+    """The same metric through the C ABI with every step's inputs copied
+    from pinned host memory and the step scalars read back every step. bf16
+    workloads: the P gradient buffers (all P rows in one pinned buffer, copied
+    in pieces of at most 1 GiB; where host memory is short, one rank's buffer
+    copied into every rank's row). MX workload: the encoded wire payload (codes and
+    scales, encoded on the GPU and parked in host memory, as a sending rank
+    would transmit them)."""
     import torch
 
-    from zero_sharded_mixed_flat_gb300 import accounting, synth
     from zero_sharded_mixed_flat_gb300 import binding as zb
 
-    n, p, ls = wl.n, wl.p, wl.loss_scale
-    opt = zb.ShardedAdamW(n, p, zb.Hparams(), torch.from_numpy(synth.init_weights(wl)))
-    if name == "staged":
-        opt.use_staged()
-        b_step = accounting.staged_shard_step_bytes_per_param() * n
+    wl, opt, stream, ls = stepper.wl, stepper.opt, stepper.stream, stepper.wl.loss_scale
+    p = wl.p
+    if wl.mx:
+        for r in range(p):
+            zb.zg_quant_mxfp8(dev[0][r], stepper.codes[r], stepper.scales[r], wl.n, stream)
+        # rows of the padded length P * S (a multiple of 32): every rank's codes stay 16-byte aligned
+        h_in = [torch.stack(stepper.codes).cpu().pin_memory(), torch.stack(stepper.scales).cpu().pin_memory()]
+        slots = [[torch.empty_like(h, device="cuda") for h in h_in] for _ in range(2)]
+        source = "MXFP8 codes + scales of the P ranks (the wire payload), one pinned buffer each"
+
+        def slot_inputs(k):
+            return slots[k]
+
+        def step_on(k):
+            c, sc = slots[k]
+            zb.zg_step_mxfp8(opt.ctx, list(c.unbind(0)), list(sc.unbind(0)), ls, stream)
     else:
-        zb.zg_set_variant(opt.ctx, zb.ZG_VARIANT_TMA)
-        b_step = accounting.shard_step_bytes_per_param(p) * n
-    for _ in range(warmup):
-        opt.step(dev, ls, stream)
-    # timed like the main line: steps issued as a caller issues them, per-pass
-    # events on every tenth step only (events between the passes keep the
-    # step pass from launching while the norm pass drains)
-    sampled = list(range(0, K, 10))
-    ev = {k: [torch.cuda.Event(enable_timing=True) for _ in range(3)] for k in sampled}
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize()
-    barrier(world)
-    e0.record(stream)
-    for k in range(K):
-        if k in ev:
-            ev[k][0].record(stream)
-            zb.zg_grad_norm(opt.ctx, dev, ls, stream)
-            ev[k][1].record(stream)
-            zb.zg_shard_step(opt.ctx, dev, ls, stream)
-            ev[k][2].record(stream)
+        slots = list(dev) + [torch.empty_like(dev[0]) for _ in range(2 - len(dev))]
+        if host is not None:
+            h_in = [host]
+            source = "P bf16 gradient buffers, one pinned buffer, copied in pieces of at most 1 GiB"
+
+            def slot_inputs(k):
+                return [slots[k].view(torch.int16)]
         else:
-            zb.zg_step(opt.ctx, dev, ls, stream)
-    e1.record(stream)
+            row = torch.empty(slots[0].shape[1], dtype=torch.int16, pin_memory=True)
+            row.copy_(dev[0][0].view(torch.int16))
+            h_in = [row] * p
+            source = ("one rank's pinned bf16 buffer copied into each of the P rank buffers "
+                      "(host memory too small for all P)")
+
+            def slot_inputs(k):
+                return [slots[k][r].view(torch.int16) for r in range(p)]
+
+        def step_on(k):
+            zb.zg_step(opt.ctx, list(slots[k].unbind(0)), ls, stream)
+
+    res = time_e2e(h_in, slot_inputs, step_on, opt, stream, max(3, min(args.steps, 200)), world)
+    return {"value": world * wl.n / res.pop("s_per_step"), "unit": UNIT,
+            "serial": world * wl.n / res.pop("serial_s_per_step"), **res,
+            "h2d_bytes_per_step": sum(h.numel() * h.element_size() for h in h_in),
+            "d2h_bytes_per_step": SCALARS_D2H_BYTES, "inputs": source}
+
+
+# --------------------------------------------------------------------- our arm
+
+def time_variant(name: str, stepper, warmup: int, K: int, samples: int, world: int, peak: float, key: str) -> dict:
+    """The same device-resident steps, on the same context and state, with
+    another bf16 variant of the library (identical results): whole-step
+    params/s and its passes' statistics. The context returns to the default
+    variant afterwards."""
+    import torch
+
+    from zero_sharded_mixed_flat_gb300 import binding as zb
+
+    opt, wl = stepper.opt, stepper.wl
+    if name == "staged":
+        if getattr(opt, "stage", None) is None:
+            opt.stage = torch.empty(wl.n, dtype=torch.float32, device="cuda")
+            zb.zg_bind_grad_stage(opt.ctx, opt.stage)
+        zb.zg_set_variant(opt.ctx, zb.ZG_VARIANT_STAGED)
+    else:
+        zb.zg_set_variant(opt.ctx, {"tma": zb.ZG_VARIANT_TMA, "single": zb.ZG_VARIANT_SINGLE}[name])
+    try:
+        for _ in range(warmup):
+            stepper.step()
+        total = time_loop(stepper, K, world)
+        # the one-launch step has no passes to time apart: its launches are timed whole
+        passes = time_whole_launches(stepper, samples) if name == "single" else time_passes(stepper, samples)
+        info = opt.info(stepper.stream)
+        assert info.status == 0 and not info.found_inf, info
+    finally:
+        zb.zg_set_variant(opt.ctx, zb.ZG_VARIANT_LDG)
+    b_step, b_norm, _ = launch_bytes(wl, "ldg" if name == "single" else name, "bf16")
+    if name == "single":
+        t = [recorded_traffic(k, key) for k in kernel_names(wl, "ldg", "bf16")]
+        kern = {"whole": pass_stats(passes["whole"], b_step + b_norm, peak, sum(t) if all(t) else None)}
+        kern["whole"]["dram_bytes_source"] = "sum of the two-launch passes' ncu DRAM bytes"
+    else:
+        kern = kernel_block(passes, wl, key, name, "bf16", peak)
+    return {"value": world * wl.n * K / total, "unit": UNIT, "ms_per_step": total * 1e3 / K,
+            "whole_step_bytes_per_param": (b_step + b_norm) / wl.n,
+            "whole_step_frac": (b_step + b_norm) * K / total / 1e9 / peak, "kernels": kern,
+            "gpu_launches": (1 if name == "single" else 2) * K}
+
+
+def time_whole_launches(stepper, samples: int) -> dict:
+    """Durations (ms) of ``samples`` whole steps, each between its own events."""
+    import torch
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(samples)]
     torch.cuda.synchronize()
+    for e in ev:
+        e[0].record(stepper.stream)
+        stepper.step()
+        e[1].record(stepper.stream)
+    torch.cuda.synchronize()
+    return {"whole": [e[0].elapsed_time(e[1]) for e in ev]}
+
+
+def bench_config(name: str, warmup: int, samples: int, peak: float, stream) -> dict:
+    """One workload in its own short loop: whole steps with a fresh gradient
+    batch every step (the workload's steps 1 and 2 alternating), the same
+    with one batch repeated (where lines left in L2 by the previous step can
+    be read again), and every pass's statistics over ``samples`` launches."""
+    import torch
+
+    from zero_sharded_mixed_flat_gb300 import binding as zb
+    from zero_sharded_mixed_flat_gb300 import synth
+
+    wl = synth.workload(name)
+    dev, _ = load_batches(wl, 2, keep_host=False)
+    opt = zb.ShardedAdamW(wl.n, wl.p, zb.Hparams(), torch.from_numpy(synth.init_weights(wl)))
+    st = Stepper(opt, wl, dev, stream)
+    for _ in range(warmup):
+        st.step()
+    K = CONFIG_STEPS[name]
+    t_fresh = time_loop(st, K, 1)
+    same = Stepper(opt, wl, dev[:1], stream)
+    t_same = time_loop(same, K, 1)
+    passes = time_passes(st, samples)
     info = opt.info(stream)
-    assert info.status == 0 and info.step_t == warmup + K
-    total = max_over_ranks(e0.elapsed_time(e1) / 1e3, world)
-    step_ms = sum(e[1].elapsed_time(e[2]) for e in ev.values()) / len(ev)
-    return {"value": world * n * K / total, "unit": UNIT, "ms_per_step": total * 1e3 / K,
-            "shard_step_us": step_ms * 1e3, "shard_step_gbs": b_step / (step_ms / 1e3) / 1e9,
-            "shard_step_bytes_per_param": b_step / n, "gpu_launches": 2 * K}
+    assert info.status == 0 and info.step_t == warmup + 2 * K + samples, info
+    b_step, b_norm, b_quant = launch_bytes(wl, "ldg", "bf16")
+    whole = b_step + b_norm + b_quant
+    kern = kernel_block(passes, wl, name, "ldg", "bf16", peak)
+    sum_us = sum(kern[k]["mean_us"] for k in kern)
+    out = {"N": wl.n, "P": wl.p, "steps": K, "value": wl.n * K / t_fresh, "unit": UNIT,
+           "ms_per_step": t_fresh * 1e3 / K, "whole_step_bytes_per_param": whole / wl.n,
+           "whole_step_gbs": whole * K / t_fresh / 1e9, "whole_step_frac": whole * K / t_fresh / 1e9 / peak,
+           "grads": "the workload's steps 1 and 2 alternating (a fresh batch every step)",
+           "same_batch": {"value": wl.n * K / t_same, "ms_per_step": t_same * 1e3 / K,
+                          "whole_step_frac": whole * K / t_same / 1e9 / peak},
+           "kernels": kern, "passes_sum_us": sum_us,
+           "overlap_us": sum_us - t_fresh * 1e6 / K}
+    del st, same, opt, dev
+    torch.cuda.empty_cache()
+    return out
 
 
 def bench_ours(args, rank: int, world: int, local: int) -> dict | None:
-    import numpy as np
     import torch
 
-    from zero_sharded_mixed_flat_gb300 import accounting, synth
+    from zero_sharded_mixed_flat_gb300 import synth
     from zero_sharded_mixed_flat_gb300 import binding as zb
 
     torch.cuda.set_device(local)
+    t_setup = time.perf_counter()
     wl = synth.workload(args.workload, **({"n": args.n} if args.n else {}))
-    n, p, ls = wl.n, wl.p, wl.loss_scale
+    key = args.workload if not args.n else f"{args.workload}@{wl.n}"
+    n, p = wl.n, wl.p
     total = synth.padded_len(wl)
     stream = torch.cuda.current_stream()
+    peak, peak_kind = measured_peaks()
+    samples = max(MIN_PASS_SAMPLES, args.kernel_samples)
 
-    # inputs resident in HBM before timing: one step's P gradient buffers
-    host = synth.step_grads(wl, 1)
-    host_t = [torch.from_numpy(h.view(np.int16)).view(torch.bfloat16) for h in host]
-    dev = [h.cuda() for h in host_t]
+    # inputs resident in HBM before timing: two batches of the P gradient
+    # buffers (one with --same-grads); with the end-to-end leg, batch 0 is
+    # drawn into pinned host memory when the host has room for it
+    local_world = int(os.environ.get("LOCAL_WORLD_SIZE", world))
+    host_bytes = p * total * 2
+    keep_host = (not args.no_e2e and not wl.mx
+                 and host_bytes + 24e9 < host_mem_available() / max(1, local_world))
+    dev, host = load_batches(wl, 1 if args.same_grads else 2, keep_host)
     opt = zb.ShardedAdamW(n, p, zb.Hparams(), torch.from_numpy(synth.init_weights(wl)), offload=args.offload)
     if args.params == "mxfp8":
         opt.use_mx_params()
     if args.variant == "staged":
         opt.use_staged()
     else:
-        zb.zg_set_variant(opt.ctx, zb.ZG_VARIANT_TMA if args.variant == "tma" else zb.ZG_VARIANT_LDG)
-    if wl.mx:
-        codes = [torch.empty(total, dtype=torch.uint8, device="cuda") for _ in range(p)]
-        scales = [torch.empty(total // 32, dtype=torch.uint8, device="cuda") for _ in range(p)]
-
-    def run_step(ev=None):
-        """One whole step; with events, mark [start, after norm, after step]
-        (the MX path adds the per-rank encodes before the norm)."""
-        if ev is None and not wl.mx:
-            zb.zg_step(opt.ctx, dev, ls, stream)
-            return
-        if ev is not None:
-            ev[0].record(stream)
-        if wl.mx:
-            for r in range(p):
-                zb.zg_quant_mxfp8(dev[r], codes[r], scales[r], n, stream)
-            if ev is not None:
-                ev[3].record(stream)
-            zb.zg_grad_norm_mxfp8(opt.ctx, codes, scales, ls, stream)
-        else:
-            zb.zg_grad_norm(opt.ctx, dev, ls, stream)
-        if ev is not None:
-            ev[1].record(stream)
-        if wl.mx:
-            zb.zg_shard_step_mxfp8(opt.ctx, codes, scales, ls, stream)
-        else:
-            zb.zg_shard_step(opt.ctx, dev, ls, stream)
-        if ev is not None:
-            ev[2].record(stream)
+        zb.zg_set_variant(opt.ctx, {"tma": zb.ZG_VARIANT_TMA, "single": zb.ZG_VARIANT_SINGLE}.get(
+            args.variant, zb.ZG_VARIANT_LDG))
+    stepper = Stepper(opt, wl, dev, stream)
+    setup_s = time.perf_counter() - t_setup
 
     for _ in range(args.warmup):
-        run_step()
+        stepper.step()
     info = opt.info(stream)
     assert info.status == 0 and not info.found_inf
 
     K = args.steps
-    # Most steps run exactly as a caller issues them (no event between the two
-    # passes, so the step pass can launch while the norm pass drains); every
-    # SAMPLE-th step is bracketed per pass with events for the kernel times.
-    SAMPLE = 10
-    sampled = list(range(0, K, SAMPLE))
-    ev = {k: [torch.cuda.Event(enable_timing=True) for _ in range(4)] for k in sampled}
-    e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local)
     clocks.start()
-    torch.cuda.synchronize()
-    barrier(world)
-    torch.cuda.synchronize()
-    clocks.region(True)
     t0 = time.perf_counter()
-    e_start.record(stream)
-    for k in range(K):
-        run_step(ev.get(k))
-    e_end.record(stream)
-    torch.cuda.synchronize()
+    t_max = time_loop(stepper, K, world, clocks)
     wall = time.perf_counter() - t0
-    clocks.region(False)
-    barrier(world)
     clk = clocks.stop()
     info = opt.info(stream)
     assert info.status == 0 and info.step_t == args.warmup + K, info
-
-    total_ms = e_start.elapsed_time(e_end)
-    norm_start = 3 if wl.mx else 0
-    norm_ms = sum(ev[k][norm_start].elapsed_time(ev[k][1]) for k in sampled) / len(sampled)
-    step_ms = sum(ev[k][1].elapsed_time(ev[k][2]) for k in sampled) / len(sampled)
-    quant_ms = sum(ev[k][0].elapsed_time(ev[k][3]) for k in sampled) / len(sampled) if wl.mx else 0.0
-    t_max = max_over_ranks(total_ms / 1e3, world)
     value = world * n * K / t_max
 
-    peak, peak_kind = measured_peaks()
-    if wl.mx and args.variant == "staged":
-        b_step = accounting.staged_shard_step_bytes_per_param() * n
-        b_norm = accounting.mx_staged_grad_norm_bytes_per_param(p) * n
-        b_quant = accounting.mx_quant_bytes_per_param() * p * n
-    elif wl.mx:
-        b_step = accounting.mx_shard_step_bytes_per_param(p) * n
-        b_norm = accounting.mx_grad_norm_bytes_per_param(p) * n
-        b_quant = accounting.mx_quant_bytes_per_param() * p * n
-    elif args.variant == "staged":
-        b_step = accounting.staged_shard_step_bytes_per_param() * n
-        b_norm = accounting.staged_grad_norm_bytes_per_param(p) * n
-        b_quant = 0.0
-    elif args.params == "mxfp8":
-        b_step = accounting.mx_params_shard_step_bytes_per_param(p) * n
-        b_norm = accounting.grad_norm_bytes_per_param(p) * n
-        b_quant = 0.0
+    # the passes' own times: `samples` more steps, every pass between its own
+    # events (the one-launch variant: every whole step between its own events)
+    single = args.variant == "single"
+    passes = time_whole_launches(stepper, samples) if single else time_passes(stepper, samples)
+    info = opt.info(stream)
+    assert info.status == 0 and info.step_t == args.warmup + K + samples, info
+    b_step, b_norm, b_quant = launch_bytes(wl, "ldg" if single else args.variant, args.params)
+    if single:
+        kern = {"whole": pass_stats(passes["whole"], b_step + b_norm, peak, None)}
+        step_kernel, sk, b_roof = "zg_step (one launch)", kern["whole"], b_step + b_norm
     else:
-        b_step = accounting.shard_step_bytes_per_param(p) * n
-        b_norm = accounting.grad_norm_bytes_per_param(p) * n
-        b_quant = 0.0
-    achieved = b_step / (step_ms / 1e3) / 1e9
+        kern = kernel_block(passes, wl, key, args.variant, args.params, peak)
+        step_kernel, _ = kernel_names(wl, args.variant, args.params)
+        sk, b_roof = kern["step"], b_step
+    whole_bytes = b_step + b_norm + b_quant
+    sum_us = sum(kern[k]["mean_us"] for k in kern)
+    kern.update(timing=f"each pass of {samples} further steps between its own CUDA events (no overlap "
+                       "between the passes); mean and spread over those launches",
+                passes_sum_us=sum_us, whole_step_us=t_max * 1e6 / K, overlap_us=sum_us - t_max * 1e6 / K,
+                whole_step_gbs=whole_bytes * K / t_max / 1e9, whole_step_frac=whole_bytes * K / t_max / 1e9 / peak)
 
-    # e2e: through the C ABI with the step's inputs coming from pinned host
-    # memory every step and the step scalars read back every step. The bf16
-    # path's inputs are the P bf16 gradient buffers; the MX path's inputs are
-    # the encoded wire payload, codes and scales (encoded once on the GPU
-    # here and parked in host memory, as a sending rank would transmit them).
-    e2e = None
-    if not args.no_e2e:
-        # the P ranks' inputs sit end to end in one pinned buffer and one
-        # device slot, so a step's host-to-device transfer is one copy per array
-        if wl.mx:
-            for r in range(p):
-                zb.zg_quant_mxfp8(dev[r], codes[r], scales[r], n, stream)
-            # rows of the padded length P * S (a multiple of 32): every rank's codes stay 16-byte aligned
-            h_in = [torch.stack(codes).cpu().pin_memory(), torch.stack(scales).cpu().pin_memory()]
-            slots = [[torch.empty_like(h, device="cuda") for h in h_in] for _ in range(2)]
+    # the other bf16 variants on the same state and inputs, then CUDA graphs
+    plain = not wl.mx and args.variant == "ldg" and not args.offload and args.params == "bf16"
+    alternatives = {}
+    if plain and not args.no_alternatives:
+        for name in ("staged", "tma", "single"):
+            alternatives[name] = time_variant(name, stepper, args.warmup, K, samples, world, peak, key)
+    graph = (time_graph(stepper, max(K, 20)) if plain and not args.no_alternatives and world == 1
+             and t_max / K < 2e-3 else None)
 
-            def slot_inputs(k):
-                return slots[k]
-
-            def step_on(k):
-                c, sc = slots[k]
-                zb.zg_step_mxfp8(opt.ctx, list(c.unbind(0)), list(sc.unbind(0)), ls, stream)
-        else:
-            h_in = [torch.stack(host_t).pin_memory()]
-            slots = [[torch.empty_like(h_in[0], device="cuda")] for _ in range(2)]
-
-            def slot_inputs(k):
-                return slots[k]
-
-            def step_on(k):
-                zb.zg_step(opt.ctx, list(slots[k][0].unbind(0)), ls, stream)
-        e2e = time_e2e(h_in, slot_inputs, step_on, opt, stream, max(3, min(K, 200)), world)
-        e2e.update(h2d_bytes_per_step=sum(h.numel() * h.element_size() for h in h_in),
-                   d2h_bytes_per_step=SCALARS_D2H_BYTES,
-                   inputs="MXFP8 codes + scales (the wire payload)" if wl.mx else "P bf16 gradient buffers")
-        e2e = {"value": world * n / e2e.pop("s_per_step"), "unit": UNIT,
-               "serial": world * n / e2e.pop("serial_s_per_step"), **e2e}
+    # end to end (refills the resident batches from host memory)
+    e2e = None if args.no_e2e else e2e_leg(stepper, dev, host, args, world)
+    del host
 
     # copy probe: achievable HBM bandwidth in the same process
     src = torch.empty(1 << 30, dtype=torch.uint8, device="cuda")
@@ -834,58 +1084,56 @@ def bench_ours(args, rank: int, world: int, local: int) -> dict | None:
         zb.zg_probe_copy(src, dst, stream)
     c1.record(stream)
     torch.cuda.synchronize()
-    probe_gbs = 2 * src.numel() * 10 / (c0.elapsed_time(c1) / 1e3) / 1e9
+    kern["probe_copy_gbs"] = 2 * src.numel() * 10 / (c0.elapsed_time(c1) / 1e3) / 1e9
     del src, dst
 
-    overlap = time_overlap(opt, wl, dev, stream, max(3, min(K, 50))) if args.overlap and not wl.mx else None
+    overlap = time_overlap(opt, wl, stepper.rows[0], stream, max(3, min(K, 50))) if args.overlap and not wl.mx else None
     stage3 = time_stage3(opt, wl, max(3, min(K, 20)), peak) if args.stage3 else None
-    graph = (time_graph(opt, dev, ls, K) if not wl.mx and args.variant == "ldg" and not args.offload
-             and args.params == "bf16" and not args.no_alternatives and world == 1 else None)
-    step_kernel = (("zg_shard_step_mxfp8" if wl.mx else "zg_shard_step")
-                   + {"staged": "_staged", "tma": "" if wl.mx else "_tma"}.get(args.variant, ""))
-    if args.params == "mxfp8":
-        step_kernel += "_mxparams"
-    alternatives = {}
-    if (not wl.mx and args.variant == "ldg" and not args.no_alternatives and not args.offload
-            and args.params == "bf16"):
-        for name in ("staged", "tma"):
-            alternatives[name] = time_variant(name, wl, dev, stream, args.warmup, K, world)
-    traffic = recorded_traffic(step_kernel, args.workload)
+    del stepper, opt, dev
+    torch.cuda.empty_cache()
+
+    configs = {}
+    if world == 1 and not args.no_configs:
+        for name in CONFIG_WORKLOADS:
+            if name != args.workload:
+                configs[name] = bench_config(name, max(args.warmup, 3), samples, peak, stream)
+
     out = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": t_max * 1e3 / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f32", "data": "synthetic (seeded bf16 gradients, resident in HBM)",
-        "config": {"workload": args.workload if not args.n else f"{args.workload} with N={n}", "N": n, "P": p,
-                   "loss_scale": ls, "variant": args.variant,
+        "dtype": "f32",
+        "data": "synthetic: seeded bf16 gradients resident in HBM, "
+                + ("one batch (the workload's step 1) every step" if args.same_grads
+                   else "the workload's steps 1 and 2 alternating (a fresh batch every step)"),
+        "config": {"workload": key, "N": n, "P": p, "loss_scale": wl.loss_scale, "variant": args.variant,
                    "optimizer_state": "pinned host memory (offloaded)" if args.offload else "HBM",
                    "params": args.params,
                    "optimizer": "AdamW lr 1e-3 b 0.9/0.999 eps 1e-8 wd 0.01 clip 1.0",
-                   "l2": f"inputs larger than L2: {(total * 2 * p + n * 14) / 1e9:.2f} GB working set vs 0.129 GB L2, no flush"},
-        "roofline": {"bound": "hbm", "kernel": step_kernel, "achieved": achieved, "peak": peak,
-                     "unit": "GB/s", "frac": achieved / peak, "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
-                     if peak_kind == "measured" else "fallback 6800 GB/s",
-                     "traffic": traffic, "algorithmic_bytes_per_launch": b_step,
-                     "bytes_per_param": b_step / n},
-        "kernels": {"timed_launches_sampled": f"every {SAMPLE}th step of the timed region",
-                    "grad_norm_us": norm_ms * 1e3, "grad_norm_gbs": b_norm / (norm_ms / 1e3) / 1e9,
-                    "shard_step_us": step_ms * 1e3, "shard_step_gbs": achieved,
-                    "whole_step_gbs": (b_step + b_norm + b_quant) / (total_ms / K / 1e3) / 1e9,
-                    "probe_copy_gbs": probe_gbs},
+                   "l2": f"inputs larger than L2: {(total * 2 * p * (1 if args.same_grads else 2) + n * 14) / 1e9:.2f} "
+                         "GB working set vs 0.129 GB L2, no flush"},
+        "roofline": {"bound": "hbm", "kernel": step_kernel, "achieved": sk["gbs"], "peak": peak,
+                     "unit": "GB/s", "frac": sk["gbs"] / peak,
+                     "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+                     else "fallback 6800 GB/s",
+                     "traffic": sk["dram_bytes"], "frac_dram": sk.get("frac_dram"),
+                     "launches_timed": samples, "duration_us": sk["mean_us"], "stdev_us": sk["stdev_us"],
+                     "algorithmic_bytes_per_launch": b_roof, "bytes_per_param": b_roof / n},
+        "kernels": kern,
         "e2e": e2e,
         "alternatives": alternatives,
         **({"overlap": overlap} if overlap else {}),
         **({"stage3": stage3} if stage3 else {}),
         **({"graph": graph} if graph else {}),
-        "gpu_launches": (2 + (p if wl.mx else 0)) * K,
+        "configs": configs,
+        "gpu_launches": ((1 if single else 2) + (p if wl.mx else 0)) * K,
         "clocks": clk,
+        "setup_s": setup_s,
         "wall_s": wall,
     }
-    if wl.mx:
-        out["kernels"].update(quant_us=quant_ms * 1e3, quant_gbs=b_quant / (quant_ms / 1e3) / 1e9)
     if args.offload:
         # the fp32 state crosses the host link twice per step (read, then written back)
         out["offload"] = {"state_bytes_over_link_per_step": 24 * n,
-                          "link_gbs_in_step_pass": 24 * n / (step_ms / 1e3) / 1e9}
+                          "link_gbs_in_step_pass": 24 * n / (sk["mean_us"] / 1e6) / 1e9}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         # the oracle on every host thread, and on one
         one = time_oracle(wl, budget_s=2.0, steps=5)
@@ -920,12 +1168,18 @@ def main(argv=None) -> int:
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="flat16m_p8")
-    ap.add_argument("--variant", choices=["ldg", "tma", "staged"], default="ldg")
+    ap.add_argument("--workload", default="flat3b_p8")
+    ap.add_argument("--variant", choices=["ldg", "tma", "staged", "single"], default="ldg")
     ap.add_argument("--n", type=int, default=None, help="override the workload's parameter count (small profiling runs)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-alternatives", action="store_true", help="skip timing the other bf16 variants")
-    ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end leg (very large workloads)")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end leg")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the other workloads' short loops (the configs sub-object)")
+    ap.add_argument("--same-grads", action="store_true",
+                    help="one resident gradient batch every step instead of two alternating")
+    ap.add_argument("--kernel-samples", type=int, default=MIN_PASS_SAMPLES,
+                    help=f"steps whose passes are timed one by one (at least {MIN_PASS_SAMPLES})")
     ap.add_argument("--params", choices=["bf16", "mxfp8"], default="bf16",
                     help="store the updated parameters as bf16 (default) or MXFP8 codes + scales")
     ap.add_argument("--overlap", action="store_true",

@@ -40,9 +40,20 @@
  *     A buffer "of n elements" must hold at least n elements; no call reads
  *     or writes an element at or past n. The shard layout pads each buffer
  *     to P * S elements; buffers that long are always large enough.
+ *   - Every pointer is checked for the kind of memory behind it
+ *     (cudaPointerGetAttributes) before anything is launched: it must be
+ *     memory of the current device (cudaMalloc, a memory pool or managed
+ *     memory), except w, m and v, which may also be pinned host memory
+ *     mapped at the same address. Ordinary host memory (malloc, the stack),
+ *     pinned host memory where device memory is needed, and another device's
+ *     memory are refused with ZG_ERR_INVALID_ARG and a message naming the
+ *     argument. The answer is remembered per pointer value, so calls that
+ *     pass the same buffers again (every step) ask the driver only once; a
+ *     buffer freed and its address handed out again as another kind of
+ *     memory is not looked at again.
  *   - A zg_stream is a cudaStream_t (NULL: the legacy default stream). Every
  *     GPU call is stream-ordered and returns without waiting, except
- *     zg_get_info and zg_set_step, which synchronise.
+ *     zg_get_info, which waits for its stream.
  *   - Return value: ZG_OK (0) or a negative ZG_ERR_* code; nothing else
  *     crosses the ABI (no exceptions). zg_strerror names a code and
  *     zg_last_error gives the calling thread's detailed message.
@@ -66,6 +77,8 @@ extern "C" {
 #define ZG_ERR_DEVICE_TIMEOUT (-5) /* a bounded device-side wait ran out (status only) */
 #define ZG_ERR_STALE_NORM (-6)     /* a shard step ran without a fresh norm pass (status only) */
 #define ZG_ERR_NO_MEMORY (-7)      /* host or device workspace allocation failed */
+#define ZG_ERR_STATE_PARTIAL (-8)  /* a bounded wait ran out after part of w, m, v and the parameters were
+                                      written (status only): restore the state from a checkpoint */
 
 #define ZG_MAX_RANKS 16
 
@@ -74,6 +87,9 @@ extern "C" {
 #define ZG_VARIANT_TMA 1    /* fused step, operands staged in a shared-memory ring by bulk async copies
                               (one producer warp, consumer warps; tile size chosen by P) */
 #define ZG_VARIANT_STAGED 2 /* the norm pass also stores the reduced fp32 gradient; the step reads it */
+#define ZG_VARIANT_SINGLE 3 /* zg_step runs the norm pass and the fused step in one cooperative launch,
+                              with a grid-wide barrier between them (the norm may differ from the
+                              two-launch norm in its last fp64 bits: its grid is its own) */
 
 typedef struct CUstream_st *zg_stream; /* same type as cudaStream_t */
 typedef struct zg_ctx zg_ctx;          /* opaque; owned by the library */
@@ -181,11 +197,16 @@ int zg_shard_step_mxfp8(zg_ctx *ctx, const uint8_t *const *codes, const uint8_t 
  * sticky device status. This is the only device-to-host read of a step. */
 int zg_get_info(zg_ctx *ctx, zg_stream stream, zg_step_info *info);
 
-/* Resume: set the applied-step count to t >= 0; the running powers b1^t and
- * b2^t are rebuilt by t multiplications from 1, as an uninterrupted run forms
- * them, so steps after a resume match an uninterrupted run bit for bit.
- * Synchronises the device; no step may be in flight on this context. */
-int zg_set_step(zg_ctx *ctx, int64_t t);
+/* Resume: set the applied-step count to t (0 <= t <= 2^62); the running
+ * powers b1^t and b2^t are rebuilt on the host by t multiplications from 1,
+ * as an uninterrupted run forms them, so steps after a resume match an
+ * uninterrupted run bit for bit. Any norm pass not yet followed by its shard
+ * step is marked consumed (it predates the resume). Stream-ordered: one
+ * single-thread kernel on `stream` writes the new values after the work
+ * already queued there; the call does not wait, and no other stream or
+ * context waits for it. Issue it on the stream that runs this context's
+ * steps (or order the streams with events). */
+int zg_set_step(zg_ctx *ctx, int64_t t, zg_stream stream);
 
 /* Store the updated parameters as MXFP8 instead of bf16 (Zero From Scratch,
  * item 14: MXFP8 takes its share off stored state; bf16 parameters and
@@ -211,18 +232,30 @@ int zg_bind_params_mxfp8(zg_ctx *ctx, uint8_t *codes, uint8_t *scales);
  * (fewer from P = 5 on). Binding only records the pointer. */
 int zg_bind_grad_stage(zg_ctx *ctx, float *stage);
 
-/* Choose how bf16 steps run: ZG_VARIANT_LDG, ZG_VARIANT_TMA or
+/* Choose how bf16 steps run: ZG_VARIANT_LDG, ZG_VARIANT_TMA,
  * ZG_VARIANT_STAGED (which needs zg_bind_grad_stage first, else
- * ZG_ERR_NOT_BOUND). The MX path follows ZG_VARIANT_STAGED too (its norm pass
- * stores the reduced gradient, its step pass reads it) and otherwise runs
- * its fused plain-load kernels. */
+ * ZG_ERR_NOT_BOUND) or ZG_VARIANT_SINGLE. The MX path follows
+ * ZG_VARIANT_STAGED too (its norm pass stores the reduced gradient, its step
+ * pass reads it) and otherwise runs its fused plain-load kernels.
+ * ZG_VARIANT_SINGLE changes zg_step only (one launch for the whole step; its
+ * grid-wide barrier waits at most the zg_set_wait_limit bound, with the same
+ * statuses as the TMA variant's waits); zg_grad_norm and zg_shard_step called
+ * on their own run the plain two-launch kernels. The TMA and one-launch
+ * variants write bf16 parameters only: with MX parameters bound they are
+ * refused. */
 int zg_set_variant(zg_ctx *ctx, int variant);
 
-/* Bound, in polls, on each device-side wait of the TMA variant (default a
- * few million, far above any healthy wait). A wait that runs out makes the
- * kernel drain its own copies, skip its remaining work and record
- * ZG_ERR_DEVICE_TIMEOUT in the status. 0 makes every first poll run out
- * (used to test that path). */
+/* Bound, in polls, on each device-side wait of the TMA variant and on the
+ * grid-wide barrier of the one-launch variant (default a few million, far
+ * above any healthy wait). A wait that runs out makes the
+ * kernel drain its own copies, skip its remaining work and leave the step
+ * uncommitted (the step count stays, the norm is consumed). The status then
+ * tells the caller what state it is in: ZG_ERR_DEVICE_TIMEOUT when no CTA
+ * had written anything yet (w, m, v and the parameters are untouched; run
+ * the norm pass and the step again), ZG_ERR_STATE_PARTIAL when some tiles
+ * had already been written (w, m, v and the parameters hold a mix of updated
+ * and old values and must be restored from a checkpoint before stepping
+ * again). 0 makes every first poll run out (used to test that path). */
 int zg_set_wait_limit(zg_ctx *ctx, int64_t polls);
 
 /* Stage three: parameters gathered just in time (DeepSpeed documentation

@@ -8,6 +8,9 @@
  * out.bin: N float32 w, N float32 m, N float32 v, N uint16 bf16 params, then
  *          for each step: double sumsq, double norm, float clip, int found_inf,
  *          int64 step_t, int status.
+ * Before the steps it checks that ordinary host memory (aligned_alloc) passed
+ * as a gradient buffer or as the master weights is refused with
+ * ZG_ERR_INVALID_ARG.
  * Exit status 0 on success; on any failure a message on stderr and 1. */
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -84,6 +87,30 @@ int main(int argc, char **argv)
 
     cudaStream_t stream;
     if (!cuda_ok(cudaStreamCreate(&stream), "stream")) return 1;
+
+    /* ordinary host memory is refused before anything is launched: as a
+     * gradient buffer, and as the master weights */
+    {
+        uint16_t *host_grad = (uint16_t *)aligned_alloc(16, len * 2);
+        float *host_w = (float *)aligned_alloc(16, len * 4);
+        const uint16_t *gh[ZG_MAX_RANKS];
+        if (!host_grad || !host_w) {
+            fprintf(stderr, "host allocation failed\n");
+            return 1;
+        }
+        for (int r = 0; r < p; ++r) gh[r] = g[r];
+        gh[p - 1] = host_grad;
+        if (zg_step(ctx, gh, loss_scale, (zg_stream)stream) != ZG_ERR_INVALID_ARG) {
+            fprintf(stderr, "a host gradient buffer was not refused\n");
+            return 1;
+        }
+        if (zg_bind(ctx, host_w, m, v, params) != ZG_ERR_INVALID_ARG) {
+            fprintf(stderr, "host master weights were not refused\n");
+            return 1;
+        }
+        free(host_grad);
+        free(host_w);
+    }
     FILE *fout = fopen(argv[6], "wb");
     if (!fout) {
         fprintf(stderr, "cannot open %s\n", argv[6]);

@@ -162,6 +162,34 @@ def test_resume_matches_uninterrupted():
     assert zb.zg_get_info(resumed.ctx).step_t == 6
 
 
+def test_resume_is_stream_ordered_and_waits_for_no_other_stream():
+    """zg_set_step is queued on the stream it is given: it returns while
+    another stream is still busy (a long chain of copies), and takes effect
+    in order on its own stream, so the next step there counts from t."""
+    w0, host = _small_case(steps=1)
+    run = GpuRun(w0, 4)
+    ref = GpuRun(w0, 4)
+    dev = [to_dev_bf16(x) for x in host[0]]
+    src = torch.empty(1 << 30, dtype=torch.uint8, device="cuda")
+    dst = torch.empty_like(src)
+    busy, mine = torch.cuda.Stream(), torch.cuda.Stream()
+    torch.cuda.synchronize()
+    for _ in range(200):  # tens of milliseconds of copying on another stream
+        zb.zg_probe_copy(src, dst, busy)
+    zb.zg_set_step(run.ctx, 5, mine)
+    zb.zg_step(run.ctx, dev, L, stream=mine)
+    assert not busy.query()  # neither call waited for the busy stream
+    info = zb.zg_get_info(run.ctx, mine)
+    assert info.status == 0 and info.step_t == 6
+    busy.synchronize()
+    # the same as resuming an idle context the same way
+    zb.zg_set_step(ref.ctx, 5)
+    zb.zg_step(ref.ctx, dev, L)
+    a, b = run.state(), ref.state()
+    for k in a:
+        assert a[k].tobytes() == b[k].tobytes(), k
+
+
 def test_loss_scale_invariance_on_gpu():
     n, p = 3001, 3
     rng = np.random.default_rng(8)

@@ -46,3 +46,24 @@ def test_gpt2_small_layout():
     assert len(t) == 148 and sum(s for _, s in t) == 124_439_808
     b = synth.buckets(124_439_808)
     assert len(b) == 5 and b[-1] == (100_000_000, 124_439_808)
+
+
+def test_generation_into_a_caller_buffer():
+    """``out=`` fills a caller's array (a row of pinned host memory, say) with
+    exactly the bits a fresh draw returns, and refuses a wrong shape or type."""
+    import pytest
+
+    w = synth.workload("flat16m_p8", n=3 * synth.CHUNK + 5)
+    total = synth.padded_len(w)
+    rows = np.zeros((2, total), dtype=np.uint16)
+    for r in range(2):
+        row = rows[r]
+        assert synth.grads_bf16(w, 1, r, 0, total, out=row) is row
+        assert np.array_equal(rows[r], synth.grads_bf16(w, 1, r, 0, total))
+    wf = np.empty(1000, np.float32)
+    synth.init_weights(w, 7, 1007, out=wf)
+    assert np.array_equal(wf, synth.init_weights(w, 7, 1007))
+    with pytest.raises(ValueError):
+        synth.grads_bf16(w, 1, 0, 0, 100, out=np.zeros(99, np.uint16))
+    with pytest.raises(ValueError):
+        synth.grads_bf16(w, 1, 0, 0, 100, out=np.zeros(100, np.int16))

@@ -28,9 +28,11 @@ ZG_ERR_CUDA = -4
 ZG_ERR_DEVICE_TIMEOUT = -5
 ZG_ERR_STALE_NORM = -6
 ZG_ERR_NO_MEMORY = -7
+ZG_ERR_STATE_PARTIAL = -8
 ZG_VARIANT_LDG = 0
 ZG_VARIANT_TMA = 1
 ZG_VARIANT_STAGED = 2
+ZG_VARIANT_SINGLE = 3
 ZG_MAX_RANKS = 16
 ZG_BUCKET_FIRST = 1
 ZG_BUCKET_LAST = 2
@@ -105,7 +107,7 @@ def lib() -> ctypes.CDLL:
             "zg_grad_norm_mxfp8": (ctypes.c_int, [_P, _P, _P, ctypes.c_float, _P]),
             "zg_shard_step_mxfp8": (ctypes.c_int, [_P, _P, _P, ctypes.c_float, _P]),
             "zg_get_info": (ctypes.c_int, [_P, _P, ctypes.POINTER(_Info)]),
-            "zg_set_step": (ctypes.c_int, [_P, _I64]),
+            "zg_set_step": (ctypes.c_int, [_P, _I64, _P]),
             "zg_set_variant": (ctypes.c_int, [_P, ctypes.c_int]),
             "zg_set_wait_limit": (ctypes.c_int, [_P, _I64]),
             "zg_probe_copy": (ctypes.c_int, [_P, _P, _I64, _P]),
@@ -307,8 +309,9 @@ def zg_get_info(ctx: Ctx, stream=None) -> StepInfo:
     return StepInfo(i.sumsq, i.norm, i.clip_coef, bool(i.found_inf), int(i.step_t), int(i.status))
 
 
-def zg_set_step(ctx: Ctx, t: int) -> None:
-    _check(lib().zg_set_step(ctx.handle, t), "zg_set_step")
+def zg_set_step(ctx: Ctx, t: int, stream=None) -> None:
+    """Resume at applied-step count t, in stream order (does not wait)."""
+    _check(lib().zg_set_step(ctx.handle, t, _stream(stream)), "zg_set_step")
 
 
 def zg_set_variant(ctx: Ctx, variant: int) -> None:

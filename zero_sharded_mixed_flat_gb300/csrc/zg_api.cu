@@ -10,6 +10,7 @@
 
 #include <map>
 #include <mutex>
+#include <unordered_map>
 #include <utility>
 
 #include "zg.h"
@@ -80,9 +81,12 @@ template <class T>
 int check_rank_ptrs(const zg_ctx *ctx, const T *const *ptrs, const char *what, bool need_align)
 {
     if (!ptrs) return fail(ZG_ERR_INVALID_ARG, "%s array is NULL", what);
+    char name[64];
     for (int r = 0; r < ctx->p; ++r) {
         if (!ptrs[r]) return fail(ZG_ERR_INVALID_ARG, "%s[%d] is NULL", what, r);
         if (need_align && !aligned16(ptrs[r])) return fail(ZG_ERR_MISALIGNED, "%s[%d] is not 16-byte aligned", what, r);
+        snprintf(name, sizeof name, "%s[%d]", what, r);
+        if (int rc = zg::check_memory(ptrs[r], false, name)) return rc;
     }
     return ZG_OK;
 }
@@ -112,7 +116,7 @@ int check_gather(const zg_ctx *ctx, int64_t lo, int64_t hi, const void *out)
     if (lo == hi) return kNothingToDo;
     if (!out) return fail(ZG_ERR_INVALID_ARG, "out is NULL");
     if (!aligned16(out)) return fail(ZG_ERR_MISALIGNED, "out must be 16-byte aligned");
-    return ZG_OK;
+    return zg::check_memory(out, false, "out");
 }
 
 int finish_launch(cudaError_t e, const char *what) { return e == cudaSuccess ? ZG_OK : cuda_fail(e, what); }
@@ -142,7 +146,93 @@ int wave_blocks(const void *kernel, int threads, size_t smem)
 
 int norm_blocks_cap() { return kPartialsCap; }
 
+// What cudaPointerGetAttributes said about a pointer the library accepted:
+// its memory type and device. Kept per pointer value so repeated calls with
+// the same buffers (every step) ask the driver once; only accepted pointers
+// are remembered, so a refused one is looked at again on its next use.
+namespace {
+struct Kind {
+    int type;
+    int device;
+};
+std::mutex g_kind_mu;
+std::unordered_map<uintptr_t, Kind> g_kinds;
+constexpr size_t kKindCacheCap = 1 << 16;
+}  // namespace
+
+// The driver's answer for one pointer, checked against what the argument
+// accepts; `a` receives the attributes.
+int classify_memory(const void *p, bool host_ok, const char *what, int dev, cudaPointerAttributes &a)
+{
+    cudaError_t e = cudaPointerGetAttributes(&a, p);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return cuda_fail(e, what);
+    }
+    switch (a.type) {
+    case cudaMemoryTypeDevice:
+    case cudaMemoryTypeManaged:
+        if (a.device != dev)
+            return fail(ZG_ERR_INVALID_ARG, "%s is memory of device %d, but the current device is %d", what, a.device,
+                        dev);
+        break;
+    case cudaMemoryTypeHost:
+        if (!host_ok)
+            return fail(ZG_ERR_INVALID_ARG, "%s is pinned host memory; it must be device memory", what);
+        if (a.devicePointer != p)
+            return fail(ZG_ERR_INVALID_ARG,
+                        "%s is pinned host memory that the device does not see at the same address "
+                        "(pin it mapped, e.g. cudaHostRegisterMapped)",
+                        what);
+        break;
+    default:
+        return fail(ZG_ERR_INVALID_ARG, "%s is not memory CUDA knows (ordinary host memory?); it must be %s", what,
+                    host_ok ? "device memory or pinned host memory" : "device memory");
+    }
+    return ZG_OK;
+}
+
+int check_memory_uncached(const void *p, bool host_ok, const char *what)
+{
+    int dev = 0;
+    const cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, what);
+    cudaPointerAttributes a;
+    return classify_memory(p, host_ok, what, dev, a);
+}
+
+int check_memory(const void *p, bool host_ok, const char *what)
+{
+    int dev = 0;
+    const cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, what);
+    const uintptr_t key = reinterpret_cast<uintptr_t>(p);
+    {
+        std::lock_guard<std::mutex> lock(g_kind_mu);
+        auto it = g_kinds.find(key);
+        if (it != g_kinds.end() && (it->second.type != cudaMemoryTypeHost || host_ok) &&
+            (it->second.type == cudaMemoryTypeHost || it->second.device == dev))
+            return ZG_OK;
+    }
+    cudaPointerAttributes a;
+    if (int rc = classify_memory(p, host_ok, what, dev, a)) return rc;
+    std::lock_guard<std::mutex> lock(g_kind_mu);
+    if (g_kinds.size() >= kKindCacheCap) g_kinds.clear();
+    g_kinds[key] = Kind{int(a.type), a.device};
+    return ZG_OK;
+}
+
 int report_error(int code, const char *msg) { return fail(code, "%s", msg); }
+
+// Resume at applied-step count t: the step count and the running powers, and
+// the pending norm (if any) marked consumed, written in stream order.
+__global__ void resume_kernel(Scalars *sc, int64_t t, double b1p, double b2p)
+{
+    sc->t = t;
+    sc->b1p = b1p;
+    sc->b2p = b2p;
+    sc->step_gen = sc->norm_gen;
+}
 
 }  // namespace zg
 
@@ -163,6 +253,7 @@ const char *zg_strerror(int code)
     case ZG_ERR_DEVICE_TIMEOUT: return "a bounded device-side wait ran out";
     case ZG_ERR_STALE_NORM: return "shard step without a fresh norm pass";
     case ZG_ERR_NO_MEMORY: return "out of memory";
+    case ZG_ERR_STATE_PARTIAL: return "a bounded device-side wait ran out after part of the state was written";
     default: return "unknown status";
     }
 }
@@ -224,6 +315,10 @@ int zg_bind(zg_ctx *ctx, float *w, float *m, float *v, uint16_t *params_bf16)
     if (!w || !m || !v || !params_bf16) return fail(ZG_ERR_INVALID_ARG, "state pointers must not be NULL");
     if (!aligned16(w) || !aligned16(m) || !aligned16(v) || !aligned16(params_bf16))
         return fail(ZG_ERR_MISALIGNED, "state pointers must be 16-byte aligned");
+    if (int rc = zg::check_memory(w, true, "w")) return rc;
+    if (int rc = zg::check_memory(m, true, "m")) return rc;
+    if (int rc = zg::check_memory(v, true, "v")) return rc;
+    if (int rc = zg::check_memory(params_bf16, false, "params")) return rc;
     ctx->w = w;
     ctx->m = m;
     ctx->v = v;
@@ -242,8 +337,11 @@ int zg_bind_params_mxfp8(zg_ctx *ctx, uint8_t *codes, uint8_t *scales)
     }
     if (!codes || !scales) return fail(ZG_ERR_INVALID_ARG, "codes and scales must both be set (or both NULL)");
     if (!aligned16(codes)) return fail(ZG_ERR_MISALIGNED, "codes must be 16-byte aligned");
-    if (ctx->variant == ZG_VARIANT_TMA)
-        return fail(ZG_ERR_INVALID_ARG, "MX parameters are written by the plain and staged step kernels, not the TMA one");
+    if (ctx->variant == ZG_VARIANT_TMA || ctx->variant == ZG_VARIANT_SINGLE)
+        return fail(ZG_ERR_INVALID_ARG,
+                    "MX parameters are written by the plain and staged step kernels, not the TMA or one-launch ones");
+    if (int rc = zg::check_memory(codes, false, "codes")) return rc;
+    if (int rc = zg::check_memory(scales, false, "scales")) return rc;
     ctx->pcodes = codes;
     ctx->pscales = scales;
     return ZG_OK;
@@ -254,6 +352,7 @@ int zg_bind_grad_stage(zg_ctx *ctx, float *stage)
     if (int rc = check_ctx(ctx, false)) return rc;
     if (!stage) return fail(ZG_ERR_INVALID_ARG, "stage must not be NULL");
     if (!aligned16(stage)) return fail(ZG_ERR_MISALIGNED, "stage must be 16-byte aligned");
+    if (int rc = zg::check_memory(stage, false, "stage")) return rc;
     ctx->stage = stage;
     return ZG_OK;
 }
@@ -327,6 +426,14 @@ int zg_shard_step(zg_ctx *ctx, const uint16_t *const *grad_ptrs, float loss_scal
 int zg_step(zg_ctx *ctx, const uint16_t *const *grad_ptrs, float loss_scale, zg_stream stream)
 {
     if (int rc = check_ctx(ctx, true)) return rc;
+    if (ctx->variant == ZG_VARIANT_SINGLE) {
+        if (int rc = check_scale(loss_scale)) return rc;
+        if (int rc = check_rank_ptrs(ctx, grad_ptrs, "grad_ptrs", true)) return rc;
+        return finish_launch(zg::launch_step_whole(ctx->p, grad_ptrs, ctx->n, inv_scale(ctx, loss_scale), ctx->k,
+                                                   state_of(ctx), ctx->d_sc, ctx->fk, ctx->d_partials,
+                                                   ctx->partials_cap, ctx->wait_limit, stream),
+                             "whole-step launch");
+    }
     if (int rc = zg_grad_norm(ctx, grad_ptrs, loss_scale, stream)) return rc;
     return zg_shard_step(ctx, grad_ptrs, loss_scale, stream);
 }
@@ -337,6 +444,9 @@ int zg_quant_mxfp8(const uint16_t *in, int64_t n, uint8_t *codes, uint8_t *scale
     if (n == 0) return ZG_OK;
     if (!in || !codes || !scales) return fail(ZG_ERR_INVALID_ARG, "pointers must not be NULL");
     if (!aligned16(in) || !aligned16(codes)) return fail(ZG_ERR_MISALIGNED, "in and codes must be 16-byte aligned");
+    if (int rc = zg::check_memory(in, false, "in")) return rc;
+    if (int rc = zg::check_memory(codes, false, "codes")) return rc;
+    if (int rc = zg::check_memory(scales, false, "scales")) return rc;
     return finish_launch(zg::launch_quant(in, n, codes, scales, stream), "MXFP8 encoder launch");
 }
 
@@ -397,33 +507,33 @@ int zg_get_info(zg_ctx *ctx, zg_stream stream, zg_step_info *info)
     return ZG_OK;
 }
 
-int zg_set_step(zg_ctx *ctx, int64_t t)
+int zg_set_step(zg_ctx *ctx, int64_t t, zg_stream stream)
 {
     if (int rc = check_ctx(ctx, false)) return rc;
-    if (t < 0) return fail(ZG_ERR_INVALID_ARG, "t must be >= 0");
+    if (t < 0 || t > (int64_t(1) << 62)) return fail(ZG_ERR_INVALID_ARG, "t must be in [0, 2^62] (got %lld)", (long long)t);
     double b1p = 1.0, b2p = 1.0;
     for (int64_t i = 0; i < t; ++i) {
         b1p = b1p * ctx->hp.beta1;
         b2p = b2p * ctx->hp.beta2;
+        if (b1p == 0.0 && b2p == 0.0) break;  // every further product is zero too
     }
-    cudaError_t e = cudaDeviceSynchronize();
-    if (e == cudaSuccess) e = cudaMemcpy(ctx->h_sc, ctx->d_sc, sizeof(zg::Scalars), cudaMemcpyDeviceToHost);
-    if (e != cudaSuccess) return cuda_fail(e, "zg_set_step read");
-    ctx->h_sc->t = t;
-    ctx->h_sc->b1p = b1p;
-    ctx->h_sc->b2p = b2p;
-    ctx->h_sc->step_gen = ctx->h_sc->norm_gen;  // any pending norm predates the resume
-    e = cudaMemcpy(ctx->d_sc, ctx->h_sc, sizeof(zg::Scalars), cudaMemcpyHostToDevice);
-    return e == cudaSuccess ? ZG_OK : cuda_fail(e, "zg_set_step write");
+    // one single-thread kernel on the caller's stream writes the step count,
+    // the running powers and marks any pending norm consumed (it predates the
+    // resume): ordered after the work already on the stream, and nothing
+    // else on the device waits for it
+    zg::resume_kernel<<<1, 1, 0, stream>>>(ctx->d_sc, t, b1p, b2p);
+    return finish_launch(cudaGetLastError(), "zg_set_step");
 }
 
 int zg_set_variant(zg_ctx *ctx, int variant)
 {
     if (int rc = check_ctx(ctx, false)) return rc;
-    if (variant != ZG_VARIANT_LDG && variant != ZG_VARIANT_TMA && variant != ZG_VARIANT_STAGED)
+    if (variant != ZG_VARIANT_LDG && variant != ZG_VARIANT_TMA && variant != ZG_VARIANT_STAGED &&
+        variant != ZG_VARIANT_SINGLE)
         return fail(ZG_ERR_INVALID_ARG, "unknown variant %d", variant);
-    if (variant == ZG_VARIANT_TMA && ctx->pcodes)
-        return fail(ZG_ERR_INVALID_ARG, "the TMA step kernel writes bf16 parameters only (MX parameters are bound)");
+    if ((variant == ZG_VARIANT_TMA || variant == ZG_VARIANT_SINGLE) && ctx->pcodes)
+        return fail(ZG_ERR_INVALID_ARG,
+                    "the TMA and one-launch step kernels write bf16 parameters only (MX parameters are bound)");
     if (variant == ZG_VARIANT_STAGED && !ctx->stage)
         return fail(ZG_ERR_NOT_BOUND, "the staged variant needs zg_bind_grad_stage first");
     ctx->variant = variant;
@@ -479,6 +589,8 @@ int zg_probe_copy(const void *src, void *dst, int64_t bytes, zg_stream stream)
     if (bytes == 0) return ZG_OK;
     if (!src || !dst) return fail(ZG_ERR_INVALID_ARG, "pointers must not be NULL");
     if (!aligned16(src) || !aligned16(dst)) return fail(ZG_ERR_MISALIGNED, "pointers must be 16-byte aligned");
+    if (int rc = zg::check_memory(src, false, "src")) return rc;
+    if (int rc = zg::check_memory(dst, false, "dst")) return rc;
     return finish_launch(zg::launch_copy(src, dst, bytes, stream), "copy probe launch");
 }
 

@@ -83,6 +83,11 @@ struct State {
 
 constexpr int kStatusTimeout = -5;     // ZG_ERR_DEVICE_TIMEOUT
 constexpr int kStatusStaleNorm = -6;   // ZG_ERR_STALE_NORM
+constexpr int kStatusPartial = -8;     // ZG_ERR_STATE_PARTIAL
+
+// step_faults: the low 31 bits count the CTAs of the current step launch
+// whose wait ran out; the top bit is set once any CTA has stored results.
+constexpr unsigned int kFaultStored = 0x80000000u;
 
 // ------------------------------------------------------------------ loads
 
@@ -166,6 +171,15 @@ __device__ __forceinline__ float2 mul_f32x2(float2 a, float2 b)
     return *reinterpret_cast<const float2 *>(&d);
 }
 
+__device__ __forceinline__ float2 add_f32x2(float2 a, float2 b)
+{
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;"
+        : "=l"(d)
+        : "l"(*reinterpret_cast<const uint64_t *>(&a)), "l"(*reinterpret_cast<const uint64_t *>(&b)));
+    return *reinterpret_cast<const float2 *>(&d);
+}
+
 __device__ __forceinline__ float2 fma_f32x2(float2 a, float2 b, float2 c)
 {
     uint64_t d;
@@ -192,6 +206,39 @@ __device__ __forceinline__ float2 e4m3x2_to_f32x2(uint16_t codes)
     uint32_t h2;
     asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(codes));
     return __half22float2(*reinterpret_cast<__half2 *>(&h2));
+}
+
+// Scale bytes whose value 2^(s - 127) is also a binary16 value (2^-24 ..
+// 2^15, subnormal below 2^-14): for these the decoded product code * scale
+// can be formed by a mixed-precision multiply-add straight from the binary16
+// code value.
+__device__ __forceinline__ bool e8m0_fits_f16(uint32_t s) { return s - 103u < 40u; }
+
+// binary16 bits of 2^(s - 127), for a byte where e8m0_fits_f16 holds.
+__device__ __forceinline__ uint16_t e8m0_as_f16(uint32_t s)
+{
+    const int e = int(s) - 127;
+    return e >= -14 ? uint16_t((e + 15) << 10) : uint16_t(1u << (e + 24));
+}
+
+// c + a * b with binary16 a, b and binary32 c, d, rounded once to binary32.
+// When a * b is exact in binary32 (a decoded E4M3 value times a power of two
+// inside binary16's range always is) this is exactly c + (a * b) rounded,
+// the rank sum's add.
+__device__ __forceinline__ float fma_f16_f32(uint16_t a, uint16_t b, float c)
+{
+    float d;
+    asm("fma.rn.f32.f16 %0, %1, %2, %3;" : "=f"(d) : "h"(a), "h"(b), "f"(c));
+    return d;
+}
+
+// Two E4M3 codes (element 2k in the low byte) to their binary16 values,
+// exact, packed (element 2k in the low half).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t codes)
+{
+    uint32_t h2;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(codes));
+    return h2;
 }
 
 // Two binary32 values to E4M3 codes, round to nearest even, saturating at
@@ -277,6 +324,9 @@ struct Bf16Src {
 template <int P>
 struct MxSrc {
     static constexpr int kRanks = P;
+#ifndef ZG_MX_F16_FMA
+#define ZG_MX_F16_FMA 1
+#endif
     const uint8_t *c[P];  // E4M3 codes, one byte per element
     const uint8_t *s[P];  // E8M0 scales, one byte per 32 elements
 
@@ -309,9 +359,32 @@ struct MxSrc {
     // overflows must read as inf before it is added.
     __device__ __forceinline__ void reduce(const Raw &raw, float (&out)[kVec]) const
     {
-        uint32_t big = 0u;
+        uint32_t big = 0u, fits = 1u;
 #pragma unroll
-        for (int r = 0; r < P; ++r) big |= uint32_t(raw.sc[r] - 247u < 8u);
+        for (int r = 0; r < P; ++r) {
+            big |= uint32_t(raw.sc[r] - 247u < 8u);
+            fits &= uint32_t(e8m0_fits_f16(raw.sc[r]));
+        }
+#if ZG_MX_F16_FMA
+        if (fits) {
+            // every scale is a binary16 power of two: one mixed-precision
+            // multiply-add per element and rank, from the binary16 code value
+#pragma unroll
+            for (int j = 0; j < kVec; ++j) out[j] = 0.0f;
+#pragma unroll
+            for (int r = 0; r < P; ++r) {
+                const uint16_t s16 = e8m0_as_f16(raw.sc[r]);
+                const uint32_t w2[2] = {raw.x[r].x, raw.x[r].y};
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const uint32_t h2 = e4m3x2_to_f16x2(uint16_t(w2[q >> 1] >> (16 * (q & 1))));
+                    out[2 * q] = fma_f16_f32(uint16_t(h2), s16, out[2 * q]);
+                    out[2 * q + 1] = fma_f16_f32(uint16_t(h2 >> 16), s16, out[2 * q + 1]);
+                }
+            }
+            return;
+        }
+#endif
         if (!big) {
             float2 acc[4];
 #pragma unroll
@@ -530,21 +603,16 @@ __device__ __forceinline__ void norm_finish(double acc, double *__restrict__ par
     }
 }
 
-// Grid-stride over 8-element vectors. Each thread owns a fixed set of
-// vectors (a function of N and the grid only), squares g in fp32, adds runs
-// of 32 squares with two-sum and widens each run to fp64; blocks reduce in a
-// fixed tree and the last block to finish sums the block partials in index
-// order. Same N, P and grid: bit-identical norm, run after run.
-template <class Src, bool kStage = false>
-__global__ void __launch_bounds__(kNormThreads, NormMinBlocks<Src>::value)
-    norm_kernel(Src src, int64_t n, float inv, double *__restrict__ partials, Scalars *sc, FinalizeK fk,
-                float *__restrict__ stage = nullptr, int mode = kNormWhole)
+// One thread's share of the norm pass: grid-stride over 8-element vectors
+// from vector `v` (stride `stride`), g squared in fp32, runs of 32 squares
+// added with two-sum and widened to fp64; block 0's thread 0 also takes the
+// ragged tail. The set of vectors, and so the sum, is a function of N, the
+// thread's index and the grid only.
+template <class Src, bool kStage>
+__device__ __forceinline__ double norm_thread_sum(const Src &src, int64_t n, float inv, float *__restrict__ stage,
+                                                  int64_t v, int64_t stride)
 {
-    pdl_wait();     // the gradients may come from the kernel just before
-    pdl_trigger();  // the step pass may start its blocks as ours retire
     const int64_t nvec = n / kVec;
-    const int64_t stride = int64_t(gridDim.x) * kNormThreads;
-    int64_t v = int64_t(blockIdx.x) * kNormThreads + threadIdx.x;
     double acc = 0.0;
     while (v < nvec) {
         const int64_t run_start = v;
@@ -610,6 +678,24 @@ __global__ void __launch_bounds__(kNormThreads, NormMinBlocks<Src>::value)
             if (kStage) stage[i] = g;
         }
     }
+    return acc;
+}
+
+// Grid-stride over 8-element vectors. Each thread owns a fixed set of
+// vectors (a function of N and the grid only), squares g in fp32, adds runs
+// of 32 squares with two-sum and widens each run to fp64; blocks reduce in a
+// fixed tree and the last block to finish sums the block partials in index
+// order. Same N, P and grid: bit-identical norm, run after run.
+template <class Src, bool kStage = false>
+__global__ void __launch_bounds__(kNormThreads, NormMinBlocks<Src>::value)
+    norm_kernel(Src src, int64_t n, float inv, double *__restrict__ partials, Scalars *sc, FinalizeK fk,
+                float *__restrict__ stage = nullptr, int mode = kNormWhole)
+{
+    pdl_wait();     // the gradients may come from the kernel just before
+    pdl_trigger();  // the step pass may start its blocks as ours retire
+    const double acc = norm_thread_sum<Src, kStage>(src, n, inv, stage,
+                                                    int64_t(blockIdx.x) * kNormThreads + threadIdx.x,
+                                                    int64_t(gridDim.x) * kNormThreads);
     norm_finish(acc, partials, sc, fk, mode);
 }
 
@@ -841,6 +927,33 @@ __device__ __forceinline__ void step_tail(const Src &src, int64_t n, float inv, 
     }
 }
 
+// One thread's share of the fused step pass over the 8-element vectors:
+// grid-stride from `v` (stride `stride`), each vector's index mirrored when
+// ZG_STEP_REVERSE walks from the end, where the norm pass finished (and its
+// last loads may still sit in L2). True when the thread stored anything.
+template <class Src>
+__device__ __forceinline__ bool step_thread_loop(const Src &src, int64_t n, float inv, float c, float bc1, float bc2,
+                                                 const StepK &k, const State &st, int64_t v, int64_t stride)
+{
+    const int64_t nvec = n / kVec;
+    constexpr int U = StepUnroll<Src>::value;
+    const bool any = v < nvec;
+#pragma unroll 1
+    for (; v < nvec; v += U * stride) {
+        VecData<Src> d[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            if (v + u * stride < nvec)
+                step_load(src, ZG_STEP_REVERSE ? nvec - 1 - (v + u * stride) : v + u * stride, st, d[u]);
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            if (v + u * stride < nvec)
+                step_compute_store(src, ZG_STEP_REVERSE ? nvec - 1 - (v + u * stride) : v + u * stride, d[u], inv,
+                                   c, bc1, bc2, k, st);
+    }
+    return any;
+}
+
 // Fused reduce-scatter + unscale + clip + AdamW + bf16 all-gather, one pass,
 // plain 128-bit loads and stores, grid-stride over 8-element vectors.
 template <class Src, bool kMxOut = false>
@@ -888,24 +1001,8 @@ __global__ void __launch_bounds__(kStepThreads, StepMinBlocks<Src>::value)
         }
         if (blockIdx.x == 0 && threadIdx.x == 0) step_tail_mx(src, n, inv, c, bc1, bc2, k, st);
     } else if (skip == 0) {
-        const int64_t nvec = n / kVec;
-        const int64_t stride = int64_t(gridDim.x) * kStepThreads;
-        constexpr int U = StepUnroll<Src>::value;
-#pragma unroll 1
-        for (int64_t v = int64_t(blockIdx.x) * kStepThreads + threadIdx.x; v < nvec; v += U * stride) {
-            VecData<Src> d[U];
-            // ZG_STEP_REVERSE walks the vectors from the end, where the norm
-            // pass finished (and its last loads may still sit in L2)
-#pragma unroll
-            for (int u = 0; u < U; ++u)
-                if (v + u * stride < nvec)
-                    step_load(src, ZG_STEP_REVERSE ? nvec - 1 - (v + u * stride) : v + u * stride, st, d[u]);
-#pragma unroll
-            for (int u = 0; u < U; ++u)
-                if (v + u * stride < nvec)
-                    step_compute_store(src, ZG_STEP_REVERSE ? nvec - 1 - (v + u * stride) : v + u * stride, d[u], inv,
-                                       c, bc1, bc2, k, st);
-        }
+        step_thread_loop(src, n, inv, c, bc1, bc2, k, st, int64_t(blockIdx.x) * kStepThreads + threadIdx.x,
+                         int64_t(gridDim.x) * kStepThreads);
         if (blockIdx.x == 0 && threadIdx.x == 0) step_tail(src, n, inv, c, bc1, bc2, k, st);
     }
     step_epilogue(sc, skip);
@@ -1092,6 +1189,7 @@ __global__ void __launch_bounds__(ws_threads(TILE), ZG_TMA_WS_MINB)
     __shared__ __align__(8) uint64_t full[8];
     __shared__ __align__(8) uint64_t empty[8];
     __shared__ int s_timeout;
+    __shared__ int s_stored;  // some consumer of this CTA has written results
     __shared__ long long s_issued;
 
     pdl_wait();
@@ -1108,6 +1206,7 @@ __global__ void __launch_bounds__(ws_threads(TILE), ZG_TMA_WS_MINB)
 
     if (threadIdx.x == 0) {
         s_timeout = 0;
+        s_stored = 0;
         s_issued = 0;
         for (int s = 0; s < stages; ++s) {
             mbar_init(&full[s], 1);
@@ -1195,6 +1294,7 @@ __global__ void __launch_bounds__(ws_threads(TILE), ZG_TMA_WS_MINB)
             // the warp's reads of buffer s are done: release it before computing
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[s]);
+            if (__any_sync(0xffffffffu, active) && lane == 0) s_stored = 1;
             if (active) {
 #pragma unroll
                 for (int q = 0; q < kVec; ++q) adamw(__fmul_rn(gh[q], inv), c, bc1, bc2, k, w[q], m[q], v[q]);
@@ -1230,17 +1330,22 @@ __global__ void __launch_bounds__(ws_threads(TILE), ZG_TMA_WS_MINB)
         skip = 3;
     } else if (skip == 0 && blockIdx.x == 0 && threadIdx.x == 0) {
         step_tail(src, n, inv, c, bc1, bc2, k, st);
+        if (n % kVec) s_stored = 1;
     }
     __syncthreads();
     // commit (or not) exactly like the plain kernel; a timeout leaves the
-    // step uncommitted and the norm consumed
+    // step uncommitted and the norm consumed. A timeout in any CTA after some
+    // CTA has stored results leaves the state half updated: that is reported
+    // as its own status, since the step cannot simply be run again.
     if (threadIdx.x == 0) {
+        if (s_stored) atomicOr(&sc->step_faults, kFaultStored);
         __threadfence();
         const unsigned int ticket = atomicAdd(&sc->step_ticket, 1u);
         if (ticket == gridDim.x - 1) {
             const unsigned int faults = atomicAdd(&sc->step_faults, 0u);
-            const int any_timeout = faults != 0u;
+            const int any_timeout = (faults & ~kFaultStored) != 0u;
             sc->step_faults = 0u;
+            if (any_timeout && (faults & kFaultStored)) sc->status = kStatusPartial;
             if (skip == 2) {
                 sc->status = kStatusStaleNorm;
             } else {

@@ -25,6 +25,11 @@ cudaError_t launch_step_bf16(int p, const uint16_t *const *g, int64_t n, float i
 cudaError_t launch_step_staged(const float *stage, int64_t n, StepK k, State state, Scalars *sc, cudaStream_t st);
 cudaError_t launch_step_tma(int p, const uint16_t *const *g, int64_t n, float inv, StepK k, State state,
                             Scalars *sc, long long wait_limit, cudaStream_t st);
+// The whole bf16 step (norm pass, grid barrier, step pass) in one cooperative
+// launch; partials holds at least max_blocks doubles.
+cudaError_t launch_step_whole(int p, const uint16_t *const *g, int64_t n, float inv, StepK k, State state,
+                              Scalars *sc, FinalizeK fk, double *partials, int max_blocks, long long wait_limit,
+                              cudaStream_t st);
 cudaError_t launch_step_mx(int p, const uint8_t *const *c, const uint8_t *const *s, int64_t n, float inv,
                            StepK k, State state, Scalars *sc, cudaStream_t st);
 cudaError_t launch_quant(const uint16_t *in, int64_t n, uint8_t *codes, uint8_t *scales, cudaStream_t st);
@@ -55,5 +60,12 @@ int norm_blocks_cap();
 // Record `msg` as the calling thread's last error text (zg_last_error) and
 // return `code`.
 int report_error(int code, const char *msg);
+
+// ZG_OK when `p` is memory of the current device (device or managed), or,
+// with `host_ok`, pinned host memory mapped at the same address; otherwise a
+// ZG_ERR_* code with a message naming `what`. Nothing is launched.
+int check_memory(const void *p, bool host_ok, const char *what);
+// The same check without remembering the answer (no host allocation).
+int check_memory_uncached(const void *p, bool host_ok, const char *what);
 
 }  // namespace zg

@@ -18,6 +18,14 @@
 // block counter) on its stream before launching. Calls that overlap on the
 // GPU (on different streams, or from different threads without ordering)
 // race on the array and give wrong results.
+//
+// The array's device address is looked up (cudaGetSymbolAddress) on the first
+// call in each CUDA context of a device and kept, with that context's id, in
+// a fixed table. A device reset (cudaDeviceReset) or a released and recreated
+// primary context loads the library's device image again, possibly at
+// another address; the next call sees a different context id and looks the
+// address up again, so it never hands the kernel the old one.
+#include <cuda.h>  // CUcontext and CUresult only: the two driver calls are found at run time
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stddef.h>
@@ -42,19 +50,62 @@ static __device__ __align__(256) unsigned char zg_noalloc_scratch[kScratchBytes]
 
 constexpr int kMaxDevices = 64;
 std::mutex g_setup_mu;
-void *g_scratch_addr[kMaxDevices];          // device address of the array, per device, once set up
-int g_wave[kMaxDevices][ZG_MAX_RANKS + 1];  // resident blocks in one wave, per device and P
+void *g_scratch_addr[kMaxDevices];               // device address of the array, per device
+unsigned long long g_scratch_ctx[kMaxDevices];   // id of the context that address belongs to
+int g_wave[kMaxDevices][ZG_MAX_RANKS + 1];       // resident blocks in one wave, per device and P
 
-// The device address of the array on `dev` (the current device). Looked up
-// once per device; the first call on a device does it.
+typedef CUresult (*CtxGetCurrentFn)(CUcontext *);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long *);
+CtxGetCurrentFn g_ctx_get_current;
+CtxGetIdFn g_ctx_get_id;
+
+// The driver's cuCtxGetCurrent and cuCtxGetId, found through the runtime
+// (the library does not link the driver library itself). Called with
+// g_setup_mu held.
+cudaError_t driver_entry_points()
+{
+    if (g_ctx_get_current && g_ctx_get_id) return cudaSuccess;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    void *fn = nullptr;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess) return e;
+    if (q != cudaDriverEntryPointSuccess || !fn) return cudaErrorSymbolNotFound;
+    g_ctx_get_current = reinterpret_cast<CtxGetCurrentFn>(fn);
+    fn = nullptr;
+    e = cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess) return e;
+    if (q != cudaDriverEntryPointSuccess || !fn) return cudaErrorSymbolNotFound;
+    g_ctx_get_id = reinterpret_cast<CtxGetIdFn>(fn);
+    return cudaSuccess;
+}
+
+// Id of the calling thread's current context, 0 when none is current yet.
+unsigned long long current_context_id()
+{
+    CUcontext c = nullptr;
+    unsigned long long id = 0;
+    if (g_ctx_get_current(&c) != CUDA_SUCCESS || !c) return 0;
+    if (g_ctx_get_id(c, &id) != CUDA_SUCCESS) return 0;
+    return id;
+}
+
+// The device address of the array on `dev` (the current device): looked up
+// by the first call in each context of the device, then reused while that
+// context stays current.
 cudaError_t scratch_on(int dev, void **addr)
 {
     std::lock_guard<std::mutex> lock(g_setup_mu);
-    if (!g_scratch_addr[dev]) {
+    cudaError_t e = driver_entry_points();
+    if (e != cudaSuccess) return e;
+    const unsigned long long id = current_context_id();
+    if (!g_scratch_addr[dev] || id == 0 || id != g_scratch_ctx[dev]) {
         void *ptr = nullptr;
-        const cudaError_t e = cudaGetSymbolAddress(&ptr, zg_noalloc_scratch);
+        e = cudaGetSymbolAddress(&ptr, zg_noalloc_scratch);  // also makes the device's primary context current
         if (e != cudaSuccess) return e;
+        const unsigned long long now = current_context_id();
+        if (now == 0) return cudaErrorDeviceUninitialized;  // no context became current
         g_scratch_addr[dev] = ptr;
+        g_scratch_ctx[dev] = now;
     }
     *addr = g_scratch_addr[dev];
     return cudaSuccess;
@@ -103,6 +154,13 @@ extern "C" int zg_grad_norm_noalloc(const uint16_t *const *grad_ptrs, int p, int
     }
     if (!out) return bad(ZG_ERR_INVALID_ARG, "out is NULL");
     if (reinterpret_cast<uintptr_t>(out) & 7u) return bad(ZG_ERR_MISALIGNED, "out must be 8-byte aligned");
+    // the kind of memory behind every pointer, asked of the driver each call
+    // (nothing is remembered, so nothing is allocated on the host either)
+    for (int r = 0; r < p; ++r) {
+        snprintf(msg, sizeof msg, "grad_ptrs[%d]", r);
+        if (int rc = zg::check_memory_uncached(grad_ptrs[r], false, msg)) return rc;
+    }
+    if (int rc = zg::check_memory_uncached(out, false, "out")) return rc;
 
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);

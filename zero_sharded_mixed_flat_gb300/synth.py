@@ -113,9 +113,13 @@ def _threads() -> int:
     return max(1, min(32, os.cpu_count() or 1))
 
 
-def _chunked(lo: int, hi: int, make_chunk, dtype) -> np.ndarray:
-    """Assemble [lo, hi) from whole seeded chunks, drawing chunks in parallel."""
-    out = np.empty(max(hi - lo, 0), dtype=dtype)
+def _chunked(lo: int, hi: int, make_chunk, dtype, out: np.ndarray | None = None) -> np.ndarray:
+    """Assemble [lo, hi) from whole seeded chunks, drawing chunks in parallel,
+    into ``out`` (hi - lo elements of ``dtype``) or a new array."""
+    if out is None:
+        out = np.empty(max(hi - lo, 0), dtype=dtype)
+    elif out.dtype != dtype or out.shape != (max(hi - lo, 0),):
+        raise ValueError(f"out must be {max(hi - lo, 0)} elements of {np.dtype(dtype)}")
     if hi <= lo:
         return out
     first, last = lo // CHUNK, (hi - 1) // CHUNK
@@ -134,14 +138,15 @@ def _chunked(lo: int, hi: int, make_chunk, dtype) -> np.ndarray:
     return out
 
 
-def init_weights(w: Workload, lo: int = 0, hi: int | None = None) -> np.ndarray:
-    """Initial fp32 master weights for flat indices [lo, hi), N(0, 0.02)."""
+def init_weights(w: Workload, lo: int = 0, hi: int | None = None, out: np.ndarray | None = None) -> np.ndarray:
+    """Initial fp32 master weights for flat indices [lo, hi), N(0, 0.02)
+    (into ``out``, float32, hi - lo elements, when given)."""
     hi = w.n if hi is None else hi
 
     def chunk(c: int) -> np.ndarray:
         return _rng(w.seed, STREAM_W, 0, 0, c).standard_normal(CHUNK, dtype=np.float32) * np.float32(0.02)
 
-    return _chunked(lo, hi, chunk, np.float32)
+    return _chunked(lo, hi, chunk, np.float32, out)
 
 
 def _grad_chunk_maker(w: Workload, step: int, rank: int):
@@ -192,10 +197,11 @@ def _to_bf16_bits(x: np.ndarray) -> np.ndarray:
 
 
 def grads_bf16(w: Workload, step: int, rank: int, lo: int = 0, hi: int | None = None,
-               loss_scale: float | None = None) -> np.ndarray:
+               loss_scale: float | None = None, out: np.ndarray | None = None) -> np.ndarray:
     """The stored gradient: bf16(f32(x) * L) on [lo, hi) (indices at or past
     N are padding and read as +0), plus the injected +inf, if any. Each
-    chunk is drawn, scaled and cast on its own worker thread."""
+    chunk is drawn, scaled and cast on its own worker thread. ``out`` (uint16,
+    hi - lo elements), when given, receives the values instead of a new array."""
     hi = w.n if hi is None else hi
     ls = np.float32(w.loss_scale if loss_scale is None else loss_scale)
     make = _grad_chunk_maker(w, step, rank)
@@ -207,7 +213,7 @@ def grads_bf16(w: Workload, step: int, rank: int, lo: int = 0, hi: int | None = 
             x[max(0, w.n - c * CHUNK):] = 0.0
         return _to_bf16_bits(x)
 
-    out = _chunked(lo, hi, chunk, np.uint16)
+    out = _chunked(lo, hi, chunk, np.uint16, out)
     k = inf_index(w, step)
     if k is not None and rank == w.inf_rank and lo <= k < hi:
         out[k - lo] = 0x7F80
