@@ -21,7 +21,7 @@ least 20 launches, each between its own CUDA events, and its bandwidth on
 the algorithmic bytes and on the DRAM bytes ncu measured; ``roofline``
 describes the fused shard-step pass against the measured HBM bandwidth;
 ``e2e`` is the same metric through the C ABI with the gradients copied from
-pinned host memory every step and the step scalars read back every step
+page-locked host memory every step and the step scalars read back every step
 (step k+1's copy overlapped with step k through two device input slots;
 ``e2e.serial`` without that overlap); ``configs`` repeats the measurement on
 the 2^24-parameter, GPT-2-small and MXFP8 workloads, each in its own short
@@ -56,6 +56,8 @@ UNIT = "params/s"
 FALLBACK_HBM_GBS = 6800.0
 SCALARS_D2H_BYTES = 112  # sizeof the device scalar block zg_get_info copies back
 COPY_PIECE = 1 << 30     # bytes per host-to-device copy in the end-to-end leg
+ALT_SECONDS = 10.0       # longest timed loop of each alternative variant
+E2E_SECONDS = 15.0       # longest timed loop of each end-to-end mode
 
 
 # --------------------------------------------------------------------- clocks
@@ -555,12 +557,37 @@ def host_mem_available() -> float:
     return float("inf")
 
 
+class RegisteredHost:
+    """A host array page-locked in place with cudaHostRegister, as a torch
+    tensor (``t``). On GB300's Grace host, copies from memory pinned this way
+    ran at the host link's rate (about 200 GB/s) at every size measured, while
+    a 48 GB buffer from the CUDA pinned allocator copied at about 72 GB/s."""
+
+    def __init__(self, shape, np_dtype, torch_dtype):
+        import numpy as np
+        import torch
+
+        self.a = np.empty(shape, dtype=np_dtype)
+        self.a.reshape(-1)[:: max(1, 4096 // self.a.itemsize)] = 0  # touch every page before locking
+        rc = int(torch.cuda.cudart().cudaHostRegister(self.a.ctypes.data, self.a.nbytes, 0))
+        if rc != 0:
+            raise RuntimeError(f"cudaHostRegister of {self.a.nbytes} bytes failed ({rc})")
+        self.t = torch.from_numpy(self.a).view(torch_dtype)
+
+    def close(self) -> None:
+        import torch
+
+        if self.a is not None:
+            torch.cuda.cudart().cudaHostUnregister(self.a.ctypes.data)
+            self.a, self.t = None, None
+
+
 def load_batches(wl, nbatch: int, keep_host: bool):
     """``nbatch`` gradient batches of the workload (its steps 1, 2, ...), each
     a device tensor [P, P*S] of bf16 whose row r is rank r's buffer, copied to
     the device before anything is timed. With ``keep_host`` batch 0 is drawn
-    straight into pinned host memory, which is returned as well (the
-    end-to-end leg copies a step's inputs from it)."""
+    straight into page-locked host memory (a RegisteredHost), which is
+    returned as well (the end-to-end leg copies a step's inputs from it)."""
     import numpy as np
     import torch
 
@@ -571,11 +598,10 @@ def load_batches(wl, nbatch: int, keep_host: bool):
     for b in range(nbatch):
         d = torch.empty((wl.p, total), dtype=torch.bfloat16, device="cuda")
         if b == 0 and keep_host:
-            host = torch.empty((wl.p, total), dtype=torch.int16, pin_memory=True)
-            hn = host.numpy().view(np.uint16)
+            host = RegisteredHost((wl.p, total), np.uint16, torch.int16)
             for r in range(wl.p):
-                synth.grads_bf16(wl, b + 1, r, 0, total, out=hn[r])
-            d.view(torch.int16).copy_(host)
+                synth.grads_bf16(wl, b + 1, r, 0, total, out=host.a[r])
+            d.view(torch.int16).copy_(host.t)
         else:
             for r in range(wl.p):
                 h = synth.grads_bf16(wl, b + 1, r, 0, total)
@@ -591,7 +617,7 @@ class Stepper:
     On the MX workload a step first encodes the P ranks' gradients (the
     wire payload), then runs the MX norm and step passes."""
 
-    def __init__(self, opt, wl, dev, stream):
+    def __init__(self, opt, wl, dev, stream, mx_fused: bool = True):
         import torch
 
         from zero_sharded_mixed_flat_gb300 import synth
@@ -599,6 +625,7 @@ class Stepper:
         self.opt, self.wl, self.stream = opt, wl, stream
         self.rows = [list(d.unbind(0)) for d in dev]
         self.k = 0
+        self.mx_fused = mx_fused
         if wl.mx:
             total = synth.padded_len(wl)
             self.codes = [torch.empty(total, dtype=torch.uint8, device="cuda") for _ in range(wl.p)]
@@ -606,7 +633,8 @@ class Stepper:
 
     def step(self, ev=None, stream=None):
         """One whole step; with events, mark [start, after norm, after step,
-        after the encodes] (the last only on the MX workload)."""
+        after the encodes] (the last only on the MX workload's separate
+        encodes; the fused encode-and-norm pass counts as the norm pass)."""
         from zero_sharded_mixed_flat_gb300 import binding as zb
 
         st = stream if stream is not None else self.stream
@@ -619,7 +647,9 @@ class Stepper:
             return
         if ev is not None:
             ev[0].record(st)
-        if self.wl.mx:
+        if self.wl.mx and self.mx_fused:
+            zb.zg_quant_norm_mxfp8(ctx, g, self.codes, self.scales, ls, st)
+        elif self.wl.mx:
             for r in range(self.wl.p):
                 zb.zg_quant_mxfp8(g[r], self.codes[r], self.scales[r], self.wl.n, st)
             if ev is not None:
@@ -671,9 +701,10 @@ def time_passes(stepper, samples: int) -> dict:
     for i in range(samples):
         stepper.step(ev[i])
     torch.cuda.synchronize()
-    n0 = 3 if stepper.wl.mx else 0
+    separate = stepper.wl.mx and not stepper.mx_fused
+    n0 = 3 if separate else 0
     out = {"norm": [e[n0].elapsed_time(e[1]) for e in ev], "step": [e[1].elapsed_time(e[2]) for e in ev]}
-    if stepper.wl.mx:
+    if separate:
         out["encode"] = [e[0].elapsed_time(e[3]) for e in ev]
     return out
 
@@ -694,11 +725,19 @@ def pass_stats(ms: list[float], bytes_per_launch: float, peak: float, traffic: f
     return st
 
 
-def launch_bytes(wl, variant: str, params: str) -> tuple[float, float, float]:
-    """Algorithmic bytes of one step pass, one norm pass and the P encodes."""
+def launch_bytes(wl, variant: str, params: str, mx_fused: bool = True) -> tuple[float, float, float]:
+    """Algorithmic bytes of one step pass, one norm pass (on the MX workload
+    with mx_fused: the pass that also encodes every rank) and the P separate
+    encodes."""
     from zero_sharded_mixed_flat_gb300 import accounting
 
     n, p = wl.n, wl.p
+    if wl.mx and mx_fused:
+        step = (accounting.staged_shard_step_bytes_per_param() if variant == "staged"
+                else accounting.mx_shard_step_bytes_per_param(p))
+        norm = (accounting.mx_staged_quant_norm_bytes_per_param(p) if variant == "staged"
+                else accounting.mx_quant_norm_bytes_per_param(p))
+        return step * n, norm * n, 0.0
     if wl.mx and variant == "staged":
         return (accounting.staged_shard_step_bytes_per_param() * n, accounting.mx_staged_grad_norm_bytes_per_param(p) * n,
                 accounting.mx_quant_bytes_per_param() * p * n)
@@ -712,20 +751,21 @@ def launch_bytes(wl, variant: str, params: str) -> tuple[float, float, float]:
     return accounting.shard_step_bytes_per_param(p) * n, accounting.grad_norm_bytes_per_param(p) * n, 0.0
 
 
-def kernel_names(wl, variant: str, params: str) -> tuple[str, str]:
+def kernel_names(wl, variant: str, params: str, mx_fused: bool = True) -> tuple[str, str]:
     """Names the ncu counters are recorded under: (step pass, norm pass)."""
     step = ("zg_shard_step_mxfp8" if wl.mx else "zg_shard_step") + \
         {"staged": "_staged", "tma": "" if wl.mx else "_tma"}.get(variant, "")
     if params == "mxfp8":
         step += "_mxparams"
-    norm = ("zg_grad_norm_mxfp8" if wl.mx else "zg_grad_norm") + ("_staged" if variant == "staged" else "")
+    norm = (("zg_quant_norm_mxfp8" if mx_fused else "zg_grad_norm_mxfp8") if wl.mx else "zg_grad_norm") + \
+        ("_staged" if variant == "staged" else "")
     return step, norm
 
 
-def kernel_block(passes: dict, wl, key: str, variant: str, params: str, peak: float) -> dict:
+def kernel_block(passes: dict, wl, key: str, variant: str, params: str, peak: float, mx_fused: bool = True) -> dict:
     """Every pass's statistics with its bandwidth (see pass_stats)."""
-    b_step, b_norm, b_quant = launch_bytes(wl, variant, params)
-    k_step, k_norm = kernel_names(wl, variant, params)
+    b_step, b_norm, b_quant = launch_bytes(wl, variant, params, mx_fused)
+    k_step, k_norm = kernel_names(wl, variant, params, mx_fused)
     out = {"step": pass_stats(passes["step"], b_step, peak, recorded_traffic(k_step, key)),
            "norm": pass_stats(passes["norm"], b_norm, peak, recorded_traffic(k_norm, key))}
     if "encode" in passes:
@@ -836,7 +876,7 @@ def time_e2e(h_in, slot_inputs, step_on, opt, stream, steps: int, world: int) ->
             "pipeline": "two device input slots; step k+1's inputs copied on a second stream during step k"}
 
 
-def e2e_leg(stepper, dev, host, args, world) -> dict:
+def e2e_leg(stepper, dev, host, args, world, step_s: float) -> dict:
     """The same metric through the C ABI with every step's inputs copied
     from pinned host memory and the step scalars read back every step. bf16
     workloads: the P gradient buffers (all P rows in one pinned buffer, copied
@@ -848,15 +888,23 @@ def e2e_leg(stepper, dev, host, args, world) -> dict:
 
     from zero_sharded_mixed_flat_gb300 import binding as zb
 
+    import numpy as np
+
     wl, opt, stream, ls = stepper.wl, stepper.opt, stepper.stream, stepper.wl.loss_scale
     p = wl.p
+    owned = []  # page-locked buffers made here, unlocked at the end
     if wl.mx:
         for r in range(p):
             zb.zg_quant_mxfp8(dev[0][r], stepper.codes[r], stepper.scales[r], wl.n, stream)
         # rows of the padded length P * S (a multiple of 32): every rank's codes stay 16-byte aligned
-        h_in = [torch.stack(stepper.codes).cpu().pin_memory(), torch.stack(stepper.scales).cpu().pin_memory()]
+        h_in = []
+        for bufs in (stepper.codes, stepper.scales):
+            h = RegisteredHost((p, bufs[0].numel()), np.uint8, torch.uint8)
+            h.t.copy_(torch.stack(bufs).cpu())
+            owned.append(h)
+            h_in.append(h.t)
         slots = [[torch.empty_like(h, device="cuda") for h in h_in] for _ in range(2)]
-        source = "MXFP8 codes + scales of the P ranks (the wire payload), one pinned buffer each"
+        source = "MXFP8 codes + scales of the P ranks (the wire payload), one page-locked buffer each"
 
         def slot_inputs(k):
             return slots[k]
@@ -867,15 +915,16 @@ def e2e_leg(stepper, dev, host, args, world) -> dict:
     else:
         slots = list(dev) + [torch.empty_like(dev[0]) for _ in range(2 - len(dev))]
         if host is not None:
-            h_in = [host]
-            source = "P bf16 gradient buffers, one pinned buffer, copied in pieces of at most 1 GiB"
+            h_in = [host.t]
+            source = "P bf16 gradient buffers, one page-locked buffer, copied in pieces of at most 1 GiB"
 
             def slot_inputs(k):
                 return [slots[k].view(torch.int16)]
         else:
-            row = torch.empty(slots[0].shape[1], dtype=torch.int16, pin_memory=True)
-            row.copy_(dev[0][0].view(torch.int16))
-            h_in = [row] * p
+            row = RegisteredHost((slots[0].shape[1],), np.uint16, torch.int16)
+            owned.append(row)
+            row.t.copy_(dev[0][0].view(torch.int16))
+            h_in = [row.t] * p
             source = ("one rank's pinned bf16 buffer copied into each of the P rank buffers "
                       "(host memory too small for all P)")
 
@@ -885,7 +934,17 @@ def e2e_leg(stepper, dev, host, args, world) -> dict:
         def step_on(k):
             zb.zg_step(opt.ctx, list(slots[k].unbind(0)), ls, stream)
 
-    res = time_e2e(h_in, slot_inputs, step_on, opt, stream, max(3, min(args.steps, 200)), world)
+    # each of the two timed loops about E2E_SECONDS long at most, at the
+    # host link's rate (K steps when shorter, 200 at most)
+    h2d = sum(h.numel() * h.element_size() for h in h_in)
+    est = h2d / 150e9 + step_s
+    try:
+        res = time_e2e(h_in, slot_inputs, step_on, opt, stream,
+                       max(3, min(args.steps, 200, int(E2E_SECONDS / est))), world)
+    finally:
+        torch.cuda.synchronize()
+        for h in owned:
+            h.close()
     return {"value": world * wl.n / res.pop("s_per_step"), "unit": UNIT,
             "serial": world * wl.n / res.pop("serial_s_per_step"), **res,
             "h2d_bytes_per_step": sum(h.numel() * h.element_size() for h in h_in),
@@ -983,6 +1042,22 @@ def bench_config(name: str, warmup: int, samples: int, peak: float, stream) -> d
                           "whole_step_frac": whole * K / t_same / 1e9 / peak},
            "kernels": kern, "passes_sum_us": sum_us,
            "overlap_us": sum_us - t_fresh * 1e6 / K}
+    if wl.mx:
+        # the same steps with the P encodes and the MX norm pass (from the
+        # stored codes) as separate launches, as a receiving rank runs them
+        sep = Stepper(opt, wl, dev, stream, mx_fused=False)
+        t_sep = time_loop(sep, K, 1)
+        p_sep = time_passes(sep, samples)
+        b_s, b_n, b_q = launch_bytes(wl, "ldg", "bf16", mx_fused=False)
+        out["separate_encode"] = {
+            "value": wl.n * K / t_sep, "ms_per_step": t_sep * 1e3 / K,
+            "whole_step_bytes_per_param": (b_s + b_n + b_q) / wl.n,
+            "whole_step_frac": (b_s + b_n + b_q) * K / t_sep / 1e9 / peak,
+            "kernels": kernel_block(p_sep, wl, name, "ldg", "bf16", peak, mx_fused=False),
+            "gpu_launches_per_step": 2 + wl.p}
+        info = opt.info(stream)
+        assert info.status == 0 and info.step_t == warmup + 3 * K + 2 * samples, info
+        del sep
     del st, same, opt, dev
     torch.cuda.empty_cache()
     return out
@@ -1063,15 +1138,20 @@ def bench_ours(args, rank: int, world: int, local: int) -> dict | None:
     # the other bf16 variants on the same state and inputs, then CUDA graphs
     plain = not wl.mx and args.variant == "ldg" and not args.offload and args.params == "bf16"
     alternatives = {}
+    step_s = t_max / K
     if plain and not args.no_alternatives:
+        # each variant's timed loop about ALT_SECONDS long at most (K steps when shorter)
+        k_alt = max(3, min(K, int(ALT_SECONDS / step_s)))
         for name in ("staged", "tma", "single"):
-            alternatives[name] = time_variant(name, stepper, args.warmup, K, samples, world, peak, key)
+            alternatives[name] = time_variant(name, stepper, min(args.warmup, k_alt), k_alt, samples, world, peak,
+                                              key)
     graph = (time_graph(stepper, max(K, 20)) if plain and not args.no_alternatives and world == 1
              and t_max / K < 2e-3 else None)
 
     # end to end (refills the resident batches from host memory)
-    e2e = None if args.no_e2e else e2e_leg(stepper, dev, host, args, world)
-    del host
+    e2e = None if args.no_e2e else e2e_leg(stepper, dev, host, args, world, step_s)
+    if host is not None:
+        host.close()
 
     # copy probe: achievable HBM bandwidth in the same process
     src = torch.empty(1 << 30, dtype=torch.uint8, device="cuda")
@@ -1125,7 +1205,7 @@ def bench_ours(args, rank: int, world: int, local: int) -> dict | None:
         **({"stage3": stage3} if stage3 else {}),
         **({"graph": graph} if graph else {}),
         "configs": configs,
-        "gpu_launches": ((1 if single else 2) + (p if wl.mx else 0)) * K,
+        "gpu_launches": (1 if single else 2) * K,
         "clocks": clk,
         "setup_s": setup_s,
         "wall_s": wall,

@@ -193,6 +193,22 @@ int zg_grad_norm_mxfp8(zg_ctx *ctx, const uint8_t *const *codes, const uint8_t *
 int zg_shard_step_mxfp8(zg_ctx *ctx, const uint8_t *const *codes, const uint8_t *const *scales,
                         float loss_scale, zg_stream stream);
 
+/* The MXFP8 wire path's encode and norm pass in one launch, for gradients
+ * that are all on this GPU: every rank's bf16 buffer grad_ptrs[r] (N
+ * elements, 16-byte aligned device memory) is encoded into codes[r] (N
+ * bytes, 16-byte aligned) and scales[r] (ceil(N/32) bytes) exactly as
+ * zg_quant_mxfp8 encodes it, and the global norm, found-inf decision and
+ * clip factor are taken from the same codes decoded in registers, exactly as
+ * zg_grad_norm_mxfp8 decodes them (its norm agrees with that pass's to
+ * rounding: the same per-element values, summed over this kernel's own
+ * grid and thread split). Follow it with zg_shard_step_mxfp8 on the same codes
+ * and scales. It reads 2P and writes P(1 + 1/32) bytes per parameter, instead
+ * of the P encodes plus a norm pass that reads the P(1 + 1/32) bytes back.
+ * With ZG_VARIANT_STAGED it also stores the reduced gradient, as the MX norm
+ * pass does. Errors as zg_grad_norm_mxfp8. */
+int zg_quant_norm_mxfp8(zg_ctx *ctx, const uint16_t *const *grad_ptrs, uint8_t *const *codes,
+                        uint8_t *const *scales, float loss_scale, zg_stream stream);
+
 /* Wait for `stream`, then copy out the step scalars. Reports and clears the
  * sticky device status. This is the only device-to-host read of a step. */
 int zg_get_info(zg_ctx *ctx, zg_stream stream, zg_step_info *info);

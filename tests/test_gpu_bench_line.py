@@ -50,7 +50,7 @@ def test_bench_line_keeps_the_contract(workload, n):
     assert roof["launches_timed"] >= bench.MIN_PASS_SAMPLES
 
     kern = line["kernels"]
-    for name in ("norm", "step") + (("encode",) if wl.mx else ()):
+    for name in ("norm", "step"):
         st = kern[name]
         assert st["launches"] >= bench.MIN_PASS_SAMPLES
         assert 0 < st["min_us"] <= st["median_us"] <= st["max_us"] and st["stdev_us"] >= 0
@@ -68,7 +68,7 @@ def test_bench_line_keeps_the_contract(workload, n):
     assert e2e["h2d_bytes_per_step"] == want_in
     assert e2e["d2h_bytes_per_step"] == 112
 
-    assert line["gpu_launches"] == (2 + (wl.p if wl.mx else 0)) * K
+    assert line["gpu_launches"] == 2 * K  # the MX workload's encodes run inside its norm pass
     clk = line["clocks"]
     assert {"sm_mhz", "sm_max_mhz", "reasons"} <= set(clk) and isinstance(clk["reasons"], list)
 
@@ -90,8 +90,10 @@ def test_bench_default_run_carries_the_other_workloads():
         wl = synth.workload(name)
         assert c["N"] == wl.n and c["P"] == wl.p and c["value"] > 0 and c["same_batch"]["value"] > 0
         assert c["ms_per_step"] == pytest.approx(wl.n / c["value"] * 1e3, rel=1e-9)
-        names = ("norm", "step") + (("encode",) if wl.mx else ())
-        assert set(names) <= set(c["kernels"])
-        for k in names:
+        assert {"norm", "step"} <= set(c["kernels"])
+        for k in ("norm", "step"):
             assert c["kernels"][k]["launches"] >= bench.MIN_PASS_SAMPLES and c["kernels"][k]["gbs"] > 0
         assert 0 < c["whole_step_frac"] < 2
+        if wl.mx:  # the separate encodes and MX norm pass, timed beside the fused one
+            sep = c["separate_encode"]
+            assert {"encode", "norm", "step"} <= set(sep["kernels"]) and sep["value"] > 0

@@ -172,3 +172,60 @@ def test_mx_step_on_lossless_gradients_equals_bf16_step(n, p):
     sa, sb = a.state(), b.state()
     for k in sa:
         assert sa[k].tobytes() == sb[k].tobytes(), k
+
+
+@pytest.mark.parametrize("n,p", [(1, 1), (7, 2), (33, 3), (1000, 8), (65_549, 8), (20_011, 11), (4096, 16),
+                                 (300_017, 4)])
+@pytest.mark.parametrize("staged", [False, True])
+def test_quant_norm_matches_encoder_separate_norm_and_oracle(n, p, staged):
+    """zg_quant_norm_mxfp8 (every rank encoded and the norm taken in one pass)
+    writes the encoder's codes and scale bytes bit for bit (the oracle's
+    encoding), makes the separate MX norm pass's decision (the same skip and
+    clip, the norm to 1e-12), and the step from its payload matches the
+    oracle, bit for bit when the clip factors agree; a step with +inf and
+    one with NaN are skipped. With the staged variant it also stores the
+    reduced gradient the staged step reads."""
+    rng = np.random.default_rng(n * 7 + p)
+    w0 = (rng.standard_normal(n) * 0.02).astype(np.float32)
+    fused, separate = GpuRun(w0, p), GpuRun(w0, p)
+    if staged:
+        for run in (fused, separate):
+            run.stage = torch.empty(n, dtype=torch.float32, device="cuda")
+            zb.zg_bind_grad_stage(run.ctx, run.stage)
+            zb.zg_set_variant(run.ctx, zb.ZG_VARIANT_STAGED)
+    ref = oracle.OracleOptimizer(w0)
+    nb = (n + 31) // 32
+    for k in range(5):
+        host = [synth.random_bf16(n, seed=800 + 10 * k + r, scale=1e-3 if k != 1 else 1.0, dist="student_t")
+                for r in range(p)]
+        if k == 2:
+            host[p - 1][n - 1] = 0x7F80
+        if k == 3:
+            host[0][0] = 0x7FC0
+        dev = [to_dev_bf16(h) for h in host]
+        codes = [Guarded(n, torch.uint8) for _ in range(p)]
+        scales = [Guarded(nb, torch.uint8) for _ in range(p)]
+        zb.zg_quant_norm_mxfp8(fused.ctx, dev, [c.view for c in codes], [s.view for s in scales], 1.0)
+        zb.zg_shard_step_mxfp8(fused.ctx, [c.view for c in codes], [s.view for s in scales], 1.0)
+        info = zb.zg_get_info(fused.ctx)
+        enc = [oracle.mx_encode(h) for h in host]
+        for r in range(p):
+            assert np.array_equal(codes[r].view.cpu().numpy(), enc[r][0]), (n, p, k, r, "codes")
+            assert np.array_equal(scales[r].view.cpu().numpy(), enc[r][1]), (n, p, k, r, "scales")
+            assert codes[r].intact() and scales[r].intact()
+        c2 = [torch.empty(n, dtype=torch.uint8, device="cuda") for _ in range(p)]
+        s2 = [torch.empty(nb, dtype=torch.uint8, device="cuda") for _ in range(p)]
+        for r in range(p):
+            zb.zg_quant_mxfp8(dev[r], c2[r], s2[r], n)
+        zb.zg_step_mxfp8(separate.ctx, c2, s2, 1.0)
+        info2 = zb.zg_get_info(separate.ctx)
+        assert info.found_inf == info2.found_inf == (k in (2, 3)), (k, info, info2)
+        if not info.found_inf:
+            assert abs(info.sumsq - info2.sumsq) <= 1e-12 * info2.sumsq, (k, info, info2)
+        dec = ref.step_mx([c for c, _ in enc], [s for _, s in enc], 1.0)
+        check_step(f"quant-norm n={n} p={p} staged={staged}", fused, ref, dec, info, k + 1)
+        if info.clip_coef == info2.clip_coef:
+            a, b = fused.state(), separate.state()
+            for key in a:
+                assert a[key].tobytes() == b[key].tobytes(), (n, p, k, key)
+    assert ref.t == 3 and fused.guards_intact()

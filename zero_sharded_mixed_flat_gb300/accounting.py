@@ -137,6 +137,17 @@ def mx_grad_norm_bytes_per_param(p: int) -> float:
     return MX_BYTES_PER_ELEMENT * p
 
 
+def mx_quant_norm_bytes_per_param(p: int) -> float:
+    """Every rank encoded and the norm taken in one pass: P bf16 reads, P code
+    + scale shares written (the norm reads nothing more)."""
+    return p * mx_quant_bytes_per_param()
+
+
+def mx_staged_quant_norm_bytes_per_param(p: int) -> float:
+    """The same pass storing the reduced fp32 gradient as well."""
+    return p * mx_quant_bytes_per_param() + 4
+
+
 def mx_staged_grad_norm_bytes_per_param(p: int) -> float:
     """MX norm pass that also stores the reduced fp32 gradient."""
     return MX_BYTES_PER_ELEMENT * p + 4

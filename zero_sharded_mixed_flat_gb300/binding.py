@@ -106,6 +106,7 @@ def lib() -> ctypes.CDLL:
             "zg_step_mxfp8": (ctypes.c_int, [_P, _P, _P, ctypes.c_float, _P]),
             "zg_grad_norm_mxfp8": (ctypes.c_int, [_P, _P, _P, ctypes.c_float, _P]),
             "zg_shard_step_mxfp8": (ctypes.c_int, [_P, _P, _P, ctypes.c_float, _P]),
+            "zg_quant_norm_mxfp8": (ctypes.c_int, [_P, _P, _P, _P, ctypes.c_float, _P]),
             "zg_get_info": (ctypes.c_int, [_P, _P, ctypes.POINTER(_Info)]),
             "zg_set_step": (ctypes.c_int, [_P, _I64, _P]),
             "zg_set_variant": (ctypes.c_int, [_P, ctypes.c_int]),
@@ -296,6 +297,14 @@ def zg_step_mxfp8(ctx: Ctx, codes, scales, loss_scale: float, stream=None) -> No
 def zg_grad_norm_mxfp8(ctx: Ctx, codes, scales, loss_scale: float, stream=None) -> None:
     c, s = _mx(ctx, codes, scales)
     _check(lib().zg_grad_norm_mxfp8(ctx.handle, c, s, loss_scale, _stream(stream)), "zg_grad_norm_mxfp8")
+
+
+def zg_quant_norm_mxfp8(ctx: Ctx, grads, codes, scales, loss_scale: float, stream=None) -> None:
+    """Encode the P bf16 gradients into ``codes``/``scales`` and take the norm
+    pass from the encoded values, in one launch."""
+    g = _grads(ctx, grads)
+    c, s = _mx(ctx, codes, scales)
+    _check(lib().zg_quant_norm_mxfp8(ctx.handle, g, c, s, loss_scale, _stream(stream)), "zg_quant_norm_mxfp8")
 
 
 def zg_shard_step_mxfp8(ctx: Ctx, codes, scales, loss_scale: float, stream=None) -> None:

@@ -463,6 +463,20 @@ int zg_grad_norm_mxfp8(zg_ctx *ctx, const uint8_t *const *codes, const uint8_t *
                          "MX norm pass launch");
 }
 
+int zg_quant_norm_mxfp8(zg_ctx *ctx, const uint16_t *const *grad_ptrs, uint8_t *const *codes,
+                        uint8_t *const *scales, float loss_scale, zg_stream stream)
+{
+    if (int rc = check_ctx(ctx, false)) return rc;
+    if (int rc = check_scale(loss_scale)) return rc;
+    if (int rc = check_rank_ptrs(ctx, grad_ptrs, "grad_ptrs", true)) return rc;
+    if (int rc = check_rank_ptrs(ctx, codes, "codes", true)) return rc;
+    if (int rc = check_rank_ptrs(ctx, scales, "scales", false)) return rc;
+    return finish_launch(zg::launch_quant_norm(ctx->p, grad_ptrs, codes, scales, ctx->n, inv_scale(ctx, loss_scale),
+                                               ctx->d_partials, ctx->partials_cap, ctx->d_sc, ctx->fk, stream,
+                                               ctx->variant == ZG_VARIANT_STAGED ? ctx->stage : nullptr),
+                         "MX encode and norm pass launch");
+}
+
 int zg_shard_step_mxfp8(zg_ctx *ctx, const uint8_t *const *codes, const uint8_t *const *scales, float loss_scale,
                         zg_stream stream)
 {

@@ -171,15 +171,6 @@ __device__ __forceinline__ float2 mul_f32x2(float2 a, float2 b)
     return *reinterpret_cast<const float2 *>(&d);
 }
 
-__device__ __forceinline__ float2 add_f32x2(float2 a, float2 b)
-{
-    uint64_t d;
-    asm("add.rn.f32x2 %0, %1, %2;"
-        : "=l"(d)
-        : "l"(*reinterpret_cast<const uint64_t *>(&a)), "l"(*reinterpret_cast<const uint64_t *>(&b)));
-    return *reinterpret_cast<const float2 *>(&d);
-}
-
 __device__ __forceinline__ float2 fma_f32x2(float2 a, float2 b, float2 c)
 {
     uint64_t d;
@@ -208,39 +199,6 @@ __device__ __forceinline__ float2 e4m3x2_to_f32x2(uint16_t codes)
     return __half22float2(*reinterpret_cast<__half2 *>(&h2));
 }
 
-// Scale bytes whose value 2^(s - 127) is also a binary16 value (2^-24 ..
-// 2^15, subnormal below 2^-14): for these the decoded product code * scale
-// can be formed by a mixed-precision multiply-add straight from the binary16
-// code value.
-__device__ __forceinline__ bool e8m0_fits_f16(uint32_t s) { return s - 103u < 40u; }
-
-// binary16 bits of 2^(s - 127), for a byte where e8m0_fits_f16 holds.
-__device__ __forceinline__ uint16_t e8m0_as_f16(uint32_t s)
-{
-    const int e = int(s) - 127;
-    return e >= -14 ? uint16_t((e + 15) << 10) : uint16_t(1u << (e + 24));
-}
-
-// c + a * b with binary16 a, b and binary32 c, d, rounded once to binary32.
-// When a * b is exact in binary32 (a decoded E4M3 value times a power of two
-// inside binary16's range always is) this is exactly c + (a * b) rounded,
-// the rank sum's add.
-__device__ __forceinline__ float fma_f16_f32(uint16_t a, uint16_t b, float c)
-{
-    float d;
-    asm("fma.rn.f32.f16 %0, %1, %2, %3;" : "=f"(d) : "h"(a), "h"(b), "f"(c));
-    return d;
-}
-
-// Two E4M3 codes (element 2k in the low byte) to their binary16 values,
-// exact, packed (element 2k in the low half).
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t codes)
-{
-    uint32_t h2;
-    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(codes));
-    return h2;
-}
-
 // Two binary32 values to E4M3 codes, round to nearest even, saturating at
 // +-448; `lo` goes to the low byte.
 __device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi)
@@ -248,6 +206,39 @@ __device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi)
     uint16_t d;
     asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(d) : "f"(hi), "f"(lo));
     return d;
+}
+
+// ------------------------------------------------------------------ MXFP8 encoder core
+
+// Sixteen bf16 values (wd: element 2k in the low half of word k; values past
+// the end of the data loaded as zero) encoded as half of one 32-element MX
+// block: this lane and its partner (lane ^ 1) hold the block's two halves,
+// so every lane of the warp must call this together. The block amax is a max
+// over the |x| bit patterns (non-negative bf16 order like unsigned
+// integers), taken on 16-bit pairs and combined across the two lanes with
+// one xor shuffle. E8M0 byte from the amax exponent field E: e = max(E - 135,
+// -127), byte = e + 127; a block holding inf or NaN gets byte 0xFF and codes
+// 0x7F. x * 2^-e is exact wherever the E4M3 rounding can see it, so the
+// packed multiply gives the codes of the scalar one. Returns the scale byte;
+// pairs[q] holds the codes of elements 2q and 2q + 1 (low byte first).
+__device__ __forceinline__ uint32_t mx_encode16(const uint32_t (&wd)[8], uint32_t (&pairs)[8])
+{
+    uint32_t m2 = 0u;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) m2 = __vmaxu2(m2, wd[q] & 0x7fff7fffu);
+    uint32_t amax = max(m2 & 0xffffu, m2 >> 16);
+    amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    const bool bad = amax >= 0x7f80u;
+    const uint32_t ex = amax >> 7;
+    const uint32_t sbyte = bad ? 0xffu : (ex > 8u ? ex - 8u : 0u);
+    const float to_unit = __uint_as_float((254u - (bad ? 0u : sbyte)) << 23);  // 2^-e
+    const float2 u2 = make_float2(to_unit, to_unit);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        const float2 y = mul_f32x2(make_float2(bf16_lo(wd[q]), bf16_hi(wd[q])), u2);
+        pairs[q] = bad ? 0x7f7fu : f32x2_to_e4m3x2(y.x, y.y);
+    }
+    return sbyte;
 }
 
 // ------------------------------------------------------------------ gradient sources
@@ -324,9 +315,6 @@ struct Bf16Src {
 template <int P>
 struct MxSrc {
     static constexpr int kRanks = P;
-#ifndef ZG_MX_F16_FMA
-#define ZG_MX_F16_FMA 1
-#endif
     const uint8_t *c[P];  // E4M3 codes, one byte per element
     const uint8_t *s[P];  // E8M0 scales, one byte per 32 elements
 
@@ -359,32 +347,9 @@ struct MxSrc {
     // overflows must read as inf before it is added.
     __device__ __forceinline__ void reduce(const Raw &raw, float (&out)[kVec]) const
     {
-        uint32_t big = 0u, fits = 1u;
+        uint32_t big = 0u;
 #pragma unroll
-        for (int r = 0; r < P; ++r) {
-            big |= uint32_t(raw.sc[r] - 247u < 8u);
-            fits &= uint32_t(e8m0_fits_f16(raw.sc[r]));
-        }
-#if ZG_MX_F16_FMA
-        if (fits) {
-            // every scale is a binary16 power of two: one mixed-precision
-            // multiply-add per element and rank, from the binary16 code value
-#pragma unroll
-            for (int j = 0; j < kVec; ++j) out[j] = 0.0f;
-#pragma unroll
-            for (int r = 0; r < P; ++r) {
-                const uint16_t s16 = e8m0_as_f16(raw.sc[r]);
-                const uint32_t w2[2] = {raw.x[r].x, raw.x[r].y};
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const uint32_t h2 = e4m3x2_to_f16x2(uint16_t(w2[q >> 1] >> (16 * (q & 1))));
-                    out[2 * q] = fma_f16_f32(uint16_t(h2), s16, out[2 * q]);
-                    out[2 * q + 1] = fma_f16_f32(uint16_t(h2 >> 16), s16, out[2 * q + 1]);
-                }
-            }
-            return;
-        }
-#endif
+        for (int r = 0; r < P; ++r) big |= uint32_t(raw.sc[r] - 247u < 8u);
         if (!big) {
             float2 acc[4];
 #pragma unroll

@@ -5,13 +5,9 @@
 // arithmetic, the scale decode and the check for scale bytes the encoder never
 // writes are paid once per sixteen elements. Decoding is issue-bound, not
 // bandwidth-bound (8.25 bytes per parameter at P = 8), which is what this
-// layout buys back. Per element: the rank-ordered fp32 sum of exact decoded
-// products, times the unscale factor, squared in fp32. The sixteen squares of
-// a vector are added in a fixed pairwise tree in fp32 (packed adds, all terms
-// non-negative, so the tree's relative error is at most four roundings), and
-// only that vector sum enters the error-free two-sum accumulation, whose
-// runs of two vectors are widened to fp64: one two-sum per sixteen elements
-// instead of one per element.
+// layout buys back. The arithmetic per element is the one norm_kernel uses:
+// the rank-ordered fp32 sum of exact decoded products, times the unscale
+// factor, squared in fp32, added in two-sum runs of 32 squares widened to fp64.
 #include "zg_launch.h"
 
 namespace zg {
@@ -26,41 +22,19 @@ struct MxNormMinBlocks {
 };
 
 // Rank-ordered sum of the decoded products for sixteen elements. Every
-// product E4M3 * 2^(s - 127) is exact in binary32 for s <= 246, so a fused
-// multiply-add gives the bits of the separate multiply and add: from the
-// binary16 code value with a binary16 scale when every rank's scale is a
-// binary16 power of two (s in 103..142, the common case), else packed in
-// binary32; a scale byte in 247..254 (never written by the encoder) takes
-// the separate operations, where an overflowing product reads as inf.
+// product E4M3 * 2^(s - 127) is exact in binary32 for s <= 246, so a packed
+// fused multiply-add gives the bits of the separate multiply and add; a scale
+// byte in 247..254 (never written by the encoder) takes the separate
+// operations, where an overflowing product reads as inf.
 template <int P>
 __device__ __forceinline__ void mx_reduce16(const uint4 (&c)[P], const uint32_t (&sb)[P], float (&out)[kMxNormVec])
 {
-    uint32_t big = 0u, fits = 1u;
+    uint32_t big = 0u;
 #pragma unroll
-    for (int r = 0; r < P; ++r) {
-        big |= uint32_t(sb[r] - 247u < 8u);
-        fits &= uint32_t(e8m0_fits_f16(sb[r]));
-    }
+    for (int r = 0; r < P; ++r) big |= uint32_t(sb[r] - 247u < 8u);
     float2 acc[kMxNormVec / 2];
 #pragma unroll
     for (int q = 0; q < kMxNormVec / 2; ++q) acc[q] = make_float2(0.0f, 0.0f);
-#if ZG_MX_F16_FMA
-    if (fits) {
-        // every scale is a binary16 power of two: one mixed-precision
-        // multiply-add per element and rank, from the binary16 code value
-#pragma unroll
-        for (int r = 0; r < P; ++r) {
-            const uint16_t s16 = e8m0_as_f16(sb[r]);
-            const uint32_t w[4] = {c[r].x, c[r].y, c[r].z, c[r].w};
-#pragma unroll
-            for (int q = 0; q < kMxNormVec / 2; ++q) {
-                const uint32_t h2 = e4m3x2_to_f16x2(uint16_t(w[q >> 1] >> (16 * (q & 1))));
-                acc[q].x = fma_f16_f32(uint16_t(h2), s16, acc[q].x);
-                acc[q].y = fma_f16_f32(uint16_t(h2 >> 16), s16, acc[q].y);
-            }
-        }
-    } else
-#endif
     if (!big) {
 #pragma unroll
         for (int r = 0; r < P; ++r) {
@@ -93,9 +67,8 @@ __device__ __forceinline__ void mx_reduce16(const uint4 (&c)[P], const uint32_t 
 
 // Grid-stride over 16-element vectors; runs of two vectors (32 squares) per
 // two-sum pair, each run widened to fp64. A run whose fp32 pair is not finite
-// (an inf or NaN square, or a tree sum that overflowed) is redone with every
-// square widened on its own, so the result is non-finite exactly when some
-// square is. Same N, P and grid: bit-identical norm.
+// is redone with every square widened on its own, so the result is non-finite
+// exactly when some square is. Same N, P and grid: bit-identical norm.
 // With kStage the pass also stores the unscaled, averaged gradient g (the
 // reduce-scatter output) for the staged step pass.
 template <int P, bool kStage>
@@ -124,21 +97,15 @@ __global__ void __launch_bounds__(kNormThreads, MxNormMinBlocks<P>::value)
             }
             float g[kMxNormVec];
             mx_reduce16<P>(c, sb, g);
-            float2 sq[kMxNormVec / 2];
 #pragma unroll
             for (int j = 0; j < kMxNormVec; j += 2) {
                 const float2 gg = mul_f32x2(make_float2(g[j], g[j + 1]), inv2);
-                sq[j / 2] = mul_f32x2(gg, gg);
+                const float2 sq = mul_f32x2(gg, gg);
+                two_sum_acc(hi, lo, sq.x);
+                two_sum_acc(hi, lo, sq.y);
                 g[j] = gg.x;
                 g[j + 1] = gg.y;
             }
-            // fixed pairwise tree over the sixteen squares
-#pragma unroll
-            for (int w = 1; w < kMxNormVec / 2; w *= 2) {
-#pragma unroll
-                for (int q = 0; q < kMxNormVec / 2; q += 2 * w) sq[q] = add_f32x2(sq[q], sq[q + w]);
-            }
-            two_sum_acc(hi, lo, __fadd_rn(sq[0].x, sq[0].y));
             if (kStage) {  // the tail the step pass reads first keeps the default policy
                 float4 *o = reinterpret_cast<float4 *>(stage) + 4 * v;
                 const bool keep = v >= nvec - kStageKeepBytes / 64;

@@ -8,12 +8,8 @@ namespace zg {
 constexpr int kQuantThreads = 256;
 constexpr int kQuantVec = 16;  // elements per thread: two 16-byte bf16 loads, one 16-byte code store
 
-// Two lanes share one 32-element block (16 elements each). The block amax is
-// a max over the |x| bit patterns (non-negative bf16 order like unsigned
-// integers), taken on 16-bit pairs and combined across the two lanes with one
-// xor shuffle. E8M0 byte from the amax exponent field E: e = max(E - 135,
-// -127), byte = e + 127. x * 2^-e is exact wherever the E4M3 rounding can see
-// it, so the packed multiply gives the codes of the scalar one.
+// Two lanes share one 32-element block (16 elements each), encoded by
+// mx_encode16.
 __global__ void __launch_bounds__(kQuantThreads)
     quant_kernel(const uint16_t *__restrict__ in, int64_t n, uint8_t *__restrict__ codes,
                  uint8_t *__restrict__ scales)
@@ -37,22 +33,8 @@ __global__ void __launch_bounds__(kQuantThreads)
             for (int j = 0; j < kQuantVec; ++j)
                 if (v * kQuantVec + j < n) wd[j >> 1] |= uint32_t(in[v * kQuantVec + j]) << (16 * (j & 1));
         }
-        uint32_t m2 = 0u;
-#pragma unroll
-        for (int q = 0; q < 8; ++q) m2 = __vmaxu2(m2, wd[q] & 0x7fff7fffu);
-        uint32_t amax = max(m2 & 0xffffu, m2 >> 16);
-        amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-        const bool bad = amax >= 0x7f80u;
-        const uint32_t ex = amax >> 7;
-        const uint32_t sbyte = bad ? 0xffu : (ex > 8u ? ex - 8u : 0u);
-        const float to_unit = __uint_as_float((254u - (bad ? 0u : sbyte)) << 23);  // 2^-e
-        const float2 u2 = make_float2(to_unit, to_unit);
         uint32_t pairs[8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            const float2 y = mul_f32x2(make_float2(bf16_lo(wd[q]), bf16_hi(wd[q])), u2);
-            pairs[q] = bad ? 0x7f7fu : f32x2_to_e4m3x2(y.x, y.y);
-        }
+        const uint32_t sbyte = mx_encode16(wd, pairs);
         if (v < nvec_full) {
             __stcs(reinterpret_cast<uint4 *>(codes) + v,
                    make_uint4(pairs[0] | (pairs[1] << 16), pairs[2] | (pairs[3] << 16), pairs[4] | (pairs[5] << 16),
