@@ -1095,7 +1095,8 @@ def bench_ours(args, rank: int, world: int, local: int) -> dict | None:
     else:
         zb.zg_set_variant(opt.ctx, {"tma": zb.ZG_VARIANT_TMA, "single": zb.ZG_VARIANT_SINGLE}.get(
             args.variant, zb.ZG_VARIANT_LDG))
-    stepper = Stepper(opt, wl, dev, stream)
+    mx_fused = not args.mx_separate
+    stepper = Stepper(opt, wl, dev, stream, mx_fused)
     setup_s = time.perf_counter() - t_setup
 
     for _ in range(args.warmup):
@@ -1120,13 +1121,13 @@ def bench_ours(args, rank: int, world: int, local: int) -> dict | None:
     passes = time_whole_launches(stepper, samples) if single else time_passes(stepper, samples)
     info = opt.info(stream)
     assert info.status == 0 and info.step_t == args.warmup + K + samples, info
-    b_step, b_norm, b_quant = launch_bytes(wl, "ldg" if single else args.variant, args.params)
+    b_step, b_norm, b_quant = launch_bytes(wl, "ldg" if single else args.variant, args.params, mx_fused)
     if single:
         kern = {"whole": pass_stats(passes["whole"], b_step + b_norm, peak, None)}
         step_kernel, sk, b_roof = "zg_step (one launch)", kern["whole"], b_step + b_norm
     else:
-        kern = kernel_block(passes, wl, key, args.variant, args.params, peak)
-        step_kernel, _ = kernel_names(wl, args.variant, args.params)
+        kern = kernel_block(passes, wl, key, args.variant, args.params, peak, mx_fused)
+        step_kernel, _ = kernel_names(wl, args.variant, args.params, mx_fused)
         sk, b_roof = kern["step"], b_step
     whole_bytes = b_step + b_norm + b_quant
     sum_us = sum(kern[k]["mean_us"] for k in kern)
@@ -1205,7 +1206,7 @@ def bench_ours(args, rank: int, world: int, local: int) -> dict | None:
         **({"stage3": stage3} if stage3 else {}),
         **({"graph": graph} if graph else {}),
         "configs": configs,
-        "gpu_launches": (1 if single else 2) * K,
+        "gpu_launches": ((1 if single else 2) + (p if wl.mx and not mx_fused else 0)) * K,
         "clocks": clk,
         "setup_s": setup_s,
         "wall_s": wall,
@@ -1262,6 +1263,8 @@ def main(argv=None) -> int:
                     help=f"steps whose passes are timed one by one (at least {MIN_PASS_SAMPLES})")
     ap.add_argument("--params", choices=["bf16", "mxfp8"], default="bf16",
                     help="store the updated parameters as bf16 (default) or MXFP8 codes + scales")
+    ap.add_argument("--mx-separate", action="store_true",
+                    help="MX workload: the P encodes and the MX norm pass as separate launches")
     ap.add_argument("--overlap", action="store_true",
                     help="also time the bucketed norm overlapped with a stand-in backward pass")
     ap.add_argument("--stage3", action="store_true",

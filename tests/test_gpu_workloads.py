@@ -95,6 +95,39 @@ def test_mxfp8_workload():
     assert ref.t == w.steps
 
 
+def test_mxfp8_workload_fused_encode_and_norm():
+    """The same workload through zg_quant_norm_mxfp8 (all eight ranks encoded
+    and the norm taken in one launch) and zg_shard_step_mxfp8: every code and
+    scale byte equals the oracle's encoding, and every step matches the
+    oracle's MX step."""
+    w = synth.workload("mxfp8_128m_p8")
+    n, p = w.n, w.p
+    total = synth.padded_len(w)
+    nb = (n + 31) // 32
+    w0 = synth.init_weights(w)
+    opt = zb.ShardedAdamW(n, p, zb.Hparams(), torch.from_numpy(w0))
+    ref = oracle.OracleOptimizer(w0)
+    dev = [torch.empty(total, dtype=torch.bfloat16, device="cuda") for _ in range(p)]
+    codes = [torch.empty(n, dtype=torch.uint8, device="cuda") for _ in range(p)]
+    scales = [torch.empty(nb, dtype=torch.uint8, device="cuda") for _ in range(p)]
+    with ThreadPoolExecutor(p) as pool:
+        for k in range(1, w.steps + 1):
+            host = [synth.grads_bf16(w, k, r) for r in range(p)]
+            ref_enc = list(pool.map(oracle.mx_encode, host))
+            for r in range(p):
+                to_dev_bf16(host[r], dev[r][:n])
+            zb.zg_quant_norm_mxfp8(opt.ctx, dev, codes, scales, w.loss_scale)
+            zb.zg_shard_step_mxfp8(opt.ctx, codes, scales, w.loss_scale)
+            info = opt.info()
+            for r in range(p):
+                gc, gs = codes[r].cpu().numpy(), scales[r].cpu().numpy()
+                assert np.array_equal(gs, ref_enc[r][1]), (k, r, int(np.sum(gs != ref_enc[r][1])))
+                assert np.array_equal(gc, ref_enc[r][0]), (k, r, int(np.sum(gc != ref_enc[r][0])))
+            dec = ref.step_mx([c for c, _ in ref_enc], [s for _, s in ref_enc], w.loss_scale)
+            _check("mxfp8_128m_p8/fused", opt, ref, dec, info, k)
+    assert ref.t == w.steps
+
+
 @pytest.mark.parametrize("name", ["flat16m_p8", "gpt2small_p8"])
 def test_variants_agree_on_full_workload(name):
     """The plain, TMA-staged and staged-gradient steps side by side on the full
