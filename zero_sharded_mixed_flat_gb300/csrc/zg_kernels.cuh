@@ -210,35 +210,44 @@ __device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi)
 
 // ------------------------------------------------------------------ MXFP8 encoder core
 
-// Sixteen bf16 values (wd: element 2k in the low half of word k; values past
-// the end of the data loaded as zero) encoded as half of one 32-element MX
-// block: this lane and its partner (lane ^ 1) hold the block's two halves,
-// so every lane of the warp must call this together. The block amax is a max
-// over the |x| bit patterns (non-negative bf16 order like unsigned
-// integers), taken on 16-bit pairs and combined across the two lanes with
-// one xor shuffle. E8M0 byte from the amax exponent field E: e = max(E - 135,
-// -127), byte = e + 127; a block holding inf or NaN gets byte 0xFF and codes
-// 0x7F. x * 2^-e is exact wherever the E4M3 rounding can see it, so the
-// packed multiply gives the codes of the scalar one. Returns the scale byte;
-// pairs[q] holds the codes of elements 2q and 2q + 1 (low byte first).
-__device__ __forceinline__ uint32_t mx_encode16(const uint32_t (&wd)[8], uint32_t (&pairs)[8])
+// A slice of one 32-element MX block, 2W bf16 values (wd: element 2k in the
+// low half of word k; values past the end of the data loaded as zero),
+// encoded by the 16 / W neighbouring lanes that hold the block's slices
+// (W = 8: two lanes of sixteen values, W = 4: four lanes of eight), so every
+// lane of the warp must call this together. The block amax is a max over the
+// |x| bit patterns (non-negative bf16 order like unsigned integers), taken on
+// 16-bit pairs and combined across the lanes with xor shuffles. E8M0 byte
+// from the amax exponent field E: e = max(E - 135, -127), byte = e + 127; a
+// block holding inf or NaN gets byte 0xFF and codes 0x7F. x * 2^-e is exact
+// wherever the E4M3 rounding can see it, so the packed multiply gives the
+// codes of the scalar one. Returns the scale byte; pairs[q] holds the codes
+// of elements 2q and 2q + 1 (low byte first).
+template <int W>
+__device__ __forceinline__ uint32_t mx_encode_slice(const uint32_t (&wd)[W], uint32_t (&pairs)[W])
 {
+    static_assert(W == 4 || W == 8, "a block is split over two or four lanes");
     uint32_t m2 = 0u;
 #pragma unroll
-    for (int q = 0; q < 8; ++q) m2 = __vmaxu2(m2, wd[q] & 0x7fff7fffu);
+    for (int q = 0; q < W; ++q) m2 = __vmaxu2(m2, wd[q] & 0x7fff7fffu);
     uint32_t amax = max(m2 & 0xffffu, m2 >> 16);
-    amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+#pragma unroll
+    for (int off = 1; off < 16 / W; off <<= 1) amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, off));
     const bool bad = amax >= 0x7f80u;
     const uint32_t ex = amax >> 7;
     const uint32_t sbyte = bad ? 0xffu : (ex > 8u ? ex - 8u : 0u);
     const float to_unit = __uint_as_float((254u - (bad ? 0u : sbyte)) << 23);  // 2^-e
     const float2 u2 = make_float2(to_unit, to_unit);
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
+    for (int q = 0; q < W; ++q) {
         const float2 y = mul_f32x2(make_float2(bf16_lo(wd[q]), bf16_hi(wd[q])), u2);
         pairs[q] = bad ? 0x7f7fu : f32x2_to_e4m3x2(y.x, y.y);
     }
     return sbyte;
+}
+
+__device__ __forceinline__ uint32_t mx_encode16(const uint32_t (&wd)[8], uint32_t (&pairs)[8])
+{
+    return mx_encode_slice<8>(wd, pairs);
 }
 
 // ------------------------------------------------------------------ gradient sources

@@ -2,59 +2,40 @@
 //
 // With every rank's bf16 gradient resident on this GPU, the encode (Zero From
 // Scratch, item 14: MXFP8 on the wire) and the norm pass that follows it can
-// share one read: per 16-element half block, each rank's bf16 values are
-// encoded exactly as zg_quant_mxfp8 encodes them (mx_encode16) and the codes
-// and scale byte stored (the wire payload the step pass reads), and the same
-// codes are decoded in registers and summed in rank order exactly as the MX
-// norm pass sums them from the payload (packed fused multiply-adds, exact
-// because each product E4M3 * 2^(s - 127) is, and the encoder never writes a
-// scale byte in 247..254). The unscaled, averaged g is squared in fp32 and
-// added with two-sum in runs of two vectors (32 squares) widened to fp64, as
-// in the MX norm pass. This saves the P * (1 + 1/32)
-// bytes per parameter the separate norm pass reads back, and P + 1 launches
-// become one.
+// share one read: per 8-element quarter block, each rank's bf16 values are
+// encoded exactly as zg_quant_mxfp8 encodes them (mx_encode_slice, the same
+// block rule over the four lanes that hold a block) and the codes and scale
+// byte stored (the wire payload the step pass reads), and the same codes are
+// decoded in registers and summed in rank order exactly as the MX norm pass
+// and the MX step pass sum them from the payload (packed fused multiply-adds,
+// exact because each product E4M3 * 2^(s - 127) is, and the encoder never
+// writes a scale byte in 247..254). The unscaled, averaged g is squared in
+// fp32 and added with two-sum in runs of four vectors (32 squares) widened to
+// fp64. This saves the P * (1 + 1/32) bytes per parameter the separate norm
+// pass reads back, and P + 1 launches become one.
 //
-// Work is split in warp-wide rows of 32 consecutive half blocks (the encoder
-// needs both halves of a block in neighbouring lanes); each thread's vectors
-// are the MX norm pass's (vector v = row + lane, rows grid-strided), and the
-// last, partial vector is read and written element by element with the
-// values past N taken as zero, as the encoder takes them.
+// Each thread issues all P ranks' 16-byte loads of its vector before encoding
+// any (P * 16 bytes in flight per thread, four 256-thread blocks per SM up to
+// P = 8). Work is split in warp-wide rows of 32 consecutive vectors (a block's
+// four quarters sit in neighbouring lanes); the last, partial vector is read
+// and written element by element with the values past N taken as zero, as
+// the encoder takes them.
 #include "zg_launch.h"
 
 namespace zg {
 
-constexpr int kQnVec = 16;
+constexpr int kQnVec = 8;     // elements per thread per vector: one 16-byte bf16 load per rank
+constexpr int kQnRun = 4;     // vectors per two-sum run (32 squares)
 
 template <int P>
 struct QuantNormMinBlocks {
-    static constexpr int value = P <= 8 ? 3 : 2;
+    static constexpr int value = P <= 8 ? 4 : 2;
 };
 
 struct MxOut {
     uint8_t *c[kMaxRanks];
     uint8_t *s[kMaxRanks];
 };
-
-// Rank r's 16 bf16 values of vector v (values at or past n as zero).
-template <int P>
-__device__ __forceinline__ void load16(const Bf16Src<P> &src, int r, int64_t v, int64_t n, uint32_t (&wd)[8])
-{
-    const int64_t nvec_full = n / kQnVec;
-    if (v < nvec_full) {
-        const uint4 a = ld_stream(reinterpret_cast<const uint4 *>(src.g[r]) + 2 * v);
-        const uint4 b = ld_stream(reinterpret_cast<const uint4 *>(src.g[r]) + 2 * v + 1);
-        wd[0] = a.x, wd[1] = a.y, wd[2] = a.z, wd[3] = a.w;
-        wd[4] = b.x, wd[5] = b.y, wd[6] = b.z, wd[7] = b.w;
-    } else {
-#pragma unroll
-        for (int q = 0; q < 8; ++q) wd[q] = 0u;
-        if (v * kQnVec < n) {
-#pragma unroll
-            for (int j = 0; j < kQnVec; ++j)
-                if (v * kQnVec + j < n) wd[j >> 1] |= uint32_t(src.g[r][v * kQnVec + j]) << (16 * (j & 1));
-        }
-    }
-}
 
 template <int P, bool kStage>
 __global__ void __launch_bounds__(kNormThreads, QuantNormMinBlocks<P>::value)
@@ -70,55 +51,58 @@ __global__ void __launch_bounds__(kNormThreads, QuantNormMinBlocks<P>::value)
     const float2 inv2 = make_float2(inv, inv);
     double acc = 0.0;
 #pragma unroll 1
-    for (int64_t row = int64_t(blockIdx.x) * kNormThreads + (threadIdx.x & ~31); row < nvec_all; row += 2 * stride) {
+    for (int64_t row = int64_t(blockIdx.x) * kNormThreads + (threadIdx.x & ~31); row < nvec_all;
+         row += kQnRun * stride) {
         float hi = 0.0f, lo = 0.0f;
 #pragma unroll 1
-        for (int k = 0; k < 2; ++k) {
+        for (int k = 0; k < kQnRun; ++k) {
             const int64_t base = row + k * stride;
             if (base >= nvec_all) break;  // warp-uniform
             const int64_t v = base + lane;
-            const bool live = v < nvec_all;
+            // every rank's values of this vector, loads issued together
+            uint32_t wd[P][4];
+            if (v < nvec_full) {
+#pragma unroll
+                for (int r = 0; r < P; ++r) {
+                    const uint4 x = ld_stream(reinterpret_cast<const uint4 *>(src.g[r]) + v);
+                    wd[r][0] = x.x, wd[r][1] = x.y, wd[r][2] = x.z, wd[r][3] = x.w;
+                }
+            } else {
+#pragma unroll
+                for (int r = 0; r < P; ++r) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) wd[r][q] = 0u;
+                    if (v < nvec_all) {
+#pragma unroll
+                        for (int j = 0; j < kQnVec; ++j)
+                            if (v * kQnVec + j < n) wd[r][j >> 1] |= uint32_t(src.g[r][v * kQnVec + j]) << (16 * (j & 1));
+                    }
+                }
+            }
             float2 g2[kQnVec / 2];
 #pragma unroll
             for (int q = 0; q < kQnVec / 2; ++q) g2[q] = make_float2(0.0f, 0.0f);
-            uint32_t cur[8], nxt[8];
-            if (live) load16(src, 0, v, n, cur);
-            else {
-#pragma unroll
-                for (int q = 0; q < 8; ++q) cur[q] = 0u;
-            }
 #pragma unroll
             for (int r = 0; r < P; ++r) {
-                if (r + 1 < P) {  // the next rank's loads in flight while this one is encoded
-                    if (live) load16(src, r + 1, v, n, nxt);
-                    else {
-#pragma unroll
-                        for (int q = 0; q < 8; ++q) nxt[q] = 0u;
-                    }
-                }
-                uint32_t pairs[8];
-                const uint32_t sbyte = mx_encode16(cur, pairs);
+                uint32_t pairs[4];
+                const uint32_t sbyte = mx_encode_slice<4>(wd[r], pairs);
                 if (v < nvec_full) {
-                    __stcs(reinterpret_cast<uint4 *>(out.c[r]) + v,
-                           make_uint4(pairs[0] | (pairs[1] << 16), pairs[2] | (pairs[3] << 16),
-                                      pairs[4] | (pairs[5] << 16), pairs[6] | (pairs[7] << 16)));
-                } else if (live) {
+                    __stcs(reinterpret_cast<uint2 *>(out.c[r]) + v,
+                           make_uint2(pairs[0] | (pairs[1] << 16), pairs[2] | (pairs[3] << 16)));
+                } else if (v < nvec_all) {
 #pragma unroll
                     for (int j = 0; j < kQnVec; ++j)
                         if (v * kQnVec + j < n) out.c[r][v * kQnVec + j] = uint8_t(pairs[j >> 1] >> (8 * (j & 1)));
                 }
-                if ((lane & 1) == 0 && live) out.s[r][v >> 1] = uint8_t(sbyte);
+                if ((lane & 3) == 0 && v < nvec_all) out.s[r][v >> 2] = uint8_t(sbyte);
                 // the decoded payload, summed in rank order
                 const float scale = e8m0_value(sbyte);
                 const float2 s2 = make_float2(scale, scale);
 #pragma unroll
                 for (int q = 0; q < kQnVec / 2; ++q) g2[q] = fma_f32x2(e4m3x2_to_f32x2(uint16_t(pairs[q])), s2, g2[q]);
-                if (r + 1 < P) {
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) cur[q] = nxt[q];
-                }
             }
-            // unscale, square in fp32, add every square with two-sum
+            // unscale, square in fp32, add every square with two-sum (vectors
+            // past the end hold zeros: their squares are +0)
 #pragma unroll
             for (int q = 0; q < kQnVec / 2; ++q) {
                 g2[q] = mul_f32x2(g2[q], inv2);
@@ -126,18 +110,18 @@ __global__ void __launch_bounds__(kNormThreads, QuantNormMinBlocks<P>::value)
                 two_sum_acc(hi, lo, sq.x);
                 two_sum_acc(hi, lo, sq.y);
             }
-            if (kStage && live) {
+            if (kStage && v < nvec_all) {
                 // the reduce-scatter output for the staged step pass
                 if (v < nvec_full) {
-                    float4 *o = reinterpret_cast<float4 *>(stage) + 4 * v;
-                    const bool keep = v >= nvec_full - kStageKeepBytes / 64;
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const float4 x = make_float4(g2[2 * q].x, g2[2 * q].y, g2[2 * q + 1].x, g2[2 * q + 1].y);
-                        if (keep)
-                            o[q] = x;
-                        else
-                            __stcs(o + q, x);
+                    float4 *o = reinterpret_cast<float4 *>(stage) + 2 * v;
+                    const float4 a = make_float4(g2[0].x, g2[0].y, g2[1].x, g2[1].y);
+                    const float4 b = make_float4(g2[2].x, g2[2].y, g2[3].x, g2[3].y);
+                    if (v >= nvec_full - kStageKeepBytes / 32) {
+                        o[0] = a;
+                        o[1] = b;
+                    } else {
+                        __stcs(o, a);
+                        __stcs(o + 1, b);
                     }
                 } else {
 #pragma unroll
@@ -147,15 +131,15 @@ __global__ void __launch_bounds__(kNormThreads, QuantNormMinBlocks<P>::value)
             }
         }
         // the codes and scale bytes of this run are written; the non-finite
-        // case below reads them back (the partner lane wrote the scale byte).
-        // Vectors past the end added zeros (their squares are +0).
+        // case below reads them back (another lane of the block wrote the
+        // scale byte)
         __syncwarp();
         if (isfinite(hi) && isfinite(lo)) {
             acc += double(hi);
             acc += double(lo);
         } else {
-            // a square that is not finite (or a run whose fp32 partial
-            // overflowed): redo the run with every square widened to fp64 on
+            // a square that is not finite, or a run whose fp32 partial
+            // overflowed: redo the run with every square widened to fp64 on
             // its own, from the payload
             MxSrc<P> mx;
 #pragma unroll
@@ -164,7 +148,7 @@ __global__ void __launch_bounds__(kNormThreads, QuantNormMinBlocks<P>::value)
                 mx.s[r] = out.s[r];
             }
 #pragma unroll 1
-            for (int k = 0; k < 2; ++k) {
+            for (int k = 0; k < kQnRun; ++k) {
                 const int64_t v = row + k * stride + lane;
                 if (v >= nvec_all) break;
 #pragma unroll 1
