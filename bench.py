@@ -559,22 +559,37 @@ def host_mem_available() -> float:
 
 class RegisteredHost:
     """A host array page-locked in place with cudaHostRegister, as a torch
-    tensor (``t``). On GB300's Grace host, copies from memory pinned this way
-    ran at the host link's rate (about 200 GB/s) at every size measured, while
-    a 48 GB buffer from the CUDA pinned allocator copied at about 72 GB/s."""
+    tensor (``t``), in memory the kernel is asked to back with transparent huge
+    pages. The GPU reads page-locked host memory through an address
+    translation per page: with the Grace host's 64 KB pages a 48 GB source is
+    some 750,000 translations and copied at 16-17 GB/s (measured), a 6 GB one
+    read eight times at 140-210 GB/s; huge pages cut the translations by four
+    orders of magnitude."""
 
     def __init__(self, shape, np_dtype, torch_dtype):
+        import mmap
+
         import numpy as np
         import torch
 
-        self.a = np.empty(shape, dtype=np_dtype)
-        self.a.reshape(-1)[:: max(1, 4096 // self.a.itemsize)] = 0  # touch every page before locking
+        count = int(np.prod(shape))
+        nbytes = count * np.dtype(np_dtype).itemsize
+        self._map = mmap.mmap(-1, max(nbytes, 1), flags=mmap.MAP_PRIVATE | mmap.MAP_ANONYMOUS)
+        self.huge = False
+        try:
+            self._map.madvise(mmap.MADV_HUGEPAGE)
+            self.huge = True
+        except (AttributeError, OSError, ValueError):
+            pass
+        self.a = np.frombuffer(self._map, dtype=np_dtype, count=count).reshape(shape)
+        self.a.reshape(-1)[:: max(1, 4096 // self.a.itemsize)] = 0  # fault every page in before locking
         rc = int(torch.cuda.cudart().cudaHostRegister(self.a.ctypes.data, self.a.nbytes, 0))
         if rc != 0:
             raise RuntimeError(f"cudaHostRegister of {self.a.nbytes} bytes failed ({rc})")
         self.t = torch.from_numpy(self.a).view(torch_dtype)
 
     def close(self) -> None:
+        """Unlock the pages (the mapping is released with the last reference)."""
         import torch
 
         if self.a is not None:
@@ -876,7 +891,7 @@ def time_e2e(h_in, slot_inputs, step_on, opt, stream, steps: int, world: int) ->
             "pipeline": "two device input slots; step k+1's inputs copied on a second stream during step k"}
 
 
-def e2e_leg(stepper, dev, host, args, world, step_s: float) -> dict:
+def e2e_leg(stepper, dev, host, max_steps: int, world, step_s: float) -> dict:
     """The same metric through the C ABI with every step's inputs copied
     from pinned host memory and the step scalars read back every step. bf16
     workloads: the P gradient buffers (all P rows in one pinned buffer, copied
@@ -940,15 +955,16 @@ def e2e_leg(stepper, dev, host, args, world, step_s: float) -> dict:
     est = h2d / 150e9 + step_s
     try:
         res = time_e2e(h_in, slot_inputs, step_on, opt, stream,
-                       max(3, min(args.steps, 200, int(E2E_SECONDS / est))), world)
+                       max(3, min(max_steps, 200, int(E2E_SECONDS / est))), world)
     finally:
         torch.cuda.synchronize()
         for h in owned:
             h.close()
-    return {"value": world * wl.n / res.pop("s_per_step"), "unit": UNIT,
-            "serial": world * wl.n / res.pop("serial_s_per_step"), **res,
-            "h2d_bytes_per_step": sum(h.numel() * h.element_size() for h in h_in),
-            "d2h_bytes_per_step": SCALARS_D2H_BYTES, "inputs": source}
+    serial = res.pop("serial_s_per_step")
+    return {"value": world * wl.n / res.pop("s_per_step"), "unit": UNIT, "serial": world * wl.n / serial, **res,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": SCALARS_D2H_BYTES, "inputs": source,
+            # the copies' own rate in the serial loop: the step's bytes over the time not spent in the step
+            "h2d_gbs_in_serial_loop": h2d / max(serial - step_s, 1e-9) / 1e9}
 
 
 # --------------------------------------------------------------------- our arm
@@ -1007,18 +1023,19 @@ def time_whole_launches(stepper, samples: int) -> dict:
     return {"whole": [e[0].elapsed_time(e[1]) for e in ev]}
 
 
-def bench_config(name: str, warmup: int, samples: int, peak: float, stream) -> dict:
+def bench_config(name: str, warmup: int, samples: int, peak: float, stream, e2e: bool = False) -> dict:
     """One workload in its own short loop: whole steps with a fresh gradient
     batch every step (the workload's steps 1 and 2 alternating), the same
     with one batch repeated (where lines left in L2 by the previous step can
-    be read again), and every pass's statistics over ``samples`` launches."""
+    be read again), and every pass's statistics over ``samples`` launches;
+    with ``e2e`` also the end-to-end leg (inputs from host memory)."""
     import torch
 
     from zero_sharded_mixed_flat_gb300 import binding as zb
     from zero_sharded_mixed_flat_gb300 import synth
 
     wl = synth.workload(name)
-    dev, _ = load_batches(wl, 2, keep_host=False)
+    dev, host = load_batches(wl, 2, keep_host=e2e and not wl.mx)
     opt = zb.ShardedAdamW(wl.n, wl.p, zb.Hparams(), torch.from_numpy(synth.init_weights(wl)))
     st = Stepper(opt, wl, dev, stream)
     for _ in range(warmup):
@@ -1058,6 +1075,10 @@ def bench_config(name: str, warmup: int, samples: int, peak: float, stream) -> d
         info = opt.info(stream)
         assert info.status == 0 and info.step_t == warmup + 3 * K + 2 * samples, info
         del sep
+    if e2e:
+        out["e2e"] = e2e_leg(st, dev, host, 200, 1, t_fresh / K)
+    if host is not None:
+        host.close()
     del st, same, opt, dev
     torch.cuda.empty_cache()
     return out
@@ -1150,7 +1171,7 @@ def bench_ours(args, rank: int, world: int, local: int) -> dict | None:
              and t_max / K < 2e-3 else None)
 
     # end to end (refills the resident batches from host memory)
-    e2e = None if args.no_e2e else e2e_leg(stepper, dev, host, args, world, step_s)
+    e2e = None if args.no_e2e else e2e_leg(stepper, dev, host, args.steps, world, step_s)
     if host is not None:
         host.close()
 
@@ -1177,7 +1198,8 @@ def bench_ours(args, rank: int, world: int, local: int) -> dict | None:
     if world == 1 and not args.no_configs:
         for name in CONFIG_WORKLOADS:
             if name != args.workload:
-                configs[name] = bench_config(name, max(args.warmup, 3), samples, peak, stream)
+                configs[name] = bench_config(name, max(args.warmup, 3), samples, peak, stream,
+                                             e2e=not args.no_e2e and name != "gpt2small_p8")
 
     out = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
