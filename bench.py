@@ -1092,8 +1092,9 @@ def bench_ours(args, rank: int, world: int, local: int) -> dict | None:
 
     torch.cuda.set_device(local)
     t_setup = time.perf_counter()
-    wl = synth.workload(args.workload, **({"n": args.n} if args.n else {}))
-    key = args.workload if not args.n else f"{args.workload}@{wl.n}"
+    over = {**({"n": args.n} if args.n else {}), **({"p": args.p} if args.p else {})}
+    wl = synth.workload(args.workload, **over)
+    key = args.workload if not over else f"{args.workload}@{wl.n}" + (f"/P={wl.p}" if args.p else "")
     n, p = wl.n, wl.p
     total = synth.padded_len(wl)
     stream = torch.cuda.current_stream()
@@ -1274,6 +1275,7 @@ def main(argv=None) -> int:
     ap.add_argument("--workload", default="flat3b_p8")
     ap.add_argument("--variant", choices=["ldg", "tma", "staged", "single"], default="ldg")
     ap.add_argument("--n", type=int, default=None, help="override the workload's parameter count (small profiling runs)")
+    ap.add_argument("--p", type=int, default=None, help="override the workload's rank count (rank-count sweeps)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-alternatives", action="store_true", help="skip timing the other bf16 variants")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end leg")
