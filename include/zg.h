@@ -339,10 +339,13 @@ int zg_probe_copy(const void *src, void *dst, int64_t bytes, zg_stream stream);
  * plus a result block); every GPU that loads the library holds that array
  * until the process exits. The first call on a device looks up the array's
  * device address (cudaGetSymbolAddress), so make that first call before any
- * stream capture. All calls on a device share the array and each clears its
- * result block and counter first: calls that overlap on the GPU race and
- * must be ordered by the caller (one stream, or events). Stream-ordered; does
- * not wait. */
+ * stream capture; after a device reset (a new CUDA context on the device) the
+ * next call looks the address up again, and should likewise come before any
+ * capture. Every pointer is checked for the kind of memory behind it, asked
+ * of the driver on every call (nothing is remembered). All calls on a device
+ * share the array and each clears its result block and counter first: calls
+ * that overlap on the GPU race and must be ordered by the caller (one stream,
+ * or events). Stream-ordered; does not wait. */
 int zg_grad_norm_noalloc(const uint16_t *const *grad_ptrs, int p, int64_t n, float loss_scale, int grad_average,
                          double *out, zg_stream stream);
 
