@@ -112,8 +112,8 @@ typedef struct {
 
 /* Create a context for N parameters over P simulated ranks (1 <= P <= 16,
  * 1 <= N < 2^62) on the current CUDA device. Allocates only a small device
- * workspace (64 KB of fp64 norm-pass block partials and a 112-byte block of
- * step scalars).
+ * workspace (64 KB of fp64 norm-pass block partials, 2 KB of counters the
+ * step pass hands out its work with, and a 112-byte block of step scalars).
  * Step count starts at 0. Layout: Zero From Scratch, item 17 (one flat
  * vector cut into P contiguous shards). *out is NULL on failure. */
 int zg_init(int64_t n, int p, const zg_hparams *hp, zg_ctx **out);
@@ -308,7 +308,7 @@ int zg_gather_params_dma(const zg_ctx *ctx, const uint16_t *const *shards, int64
  * value code * 2^(scale - 127) and rounded to bf16 (nearest even; this only
  * acts below 2^-126, since a decoded value has at most four significant
  * bits); a NaN code or scale gathers as 0x7FC0. An lo that is a multiple of
- * 16 takes the vector path. Reads 1 + 1/32 and writes 2 bytes per gathered
+ * 8 takes the vector path (8 codes in, one 16-byte store out). Reads 1 + 1/32 and writes 2 bytes per gathered
  * parameter. Errors as zg_gather_params. */
 int zg_gather_params_mxfp8(const zg_ctx *ctx, const uint8_t *const *codes, const uint8_t *const *scales, int64_t lo,
                            int64_t hi, uint16_t *out, zg_stream stream);

@@ -35,6 +35,7 @@ struct zg_ctx {
     zg::Scalars *d_sc;
     double *d_partials;
     int partials_cap;
+    unsigned long long *d_work;  // the step pass's chunk counters (zg::kWorkWords words)
     zg::Scalars *h_sc;
     int variant;
     long long wait_limit;
@@ -99,7 +100,7 @@ float inv_scale(const zg_ctx *ctx, float loss_scale)
 
 zg::State state_of(const zg_ctx *ctx)
 {
-    return zg::State{ctx->w, ctx->m, ctx->v, ctx->params, ctx->pcodes, ctx->pscales};
+    return zg::State{ctx->w, ctx->m, ctx->v, ctx->params, ctx->pcodes, ctx->pscales, ctx->d_work};
 }
 
 // Checks shared by the gathers: a context, a range inside [0, N) and a
@@ -289,6 +290,8 @@ int zg_init(int64_t n, int p, const zg_hparams *hp, zg_ctx **out)
     cudaError_t e = cudaGetDevice(&ctx->device);
     if (e == cudaSuccess) e = cudaMalloc(&ctx->d_sc, sizeof(zg::Scalars));
     if (e == cudaSuccess) e = cudaMalloc(&ctx->d_partials, sizeof(double) * ctx->partials_cap);
+    if (e == cudaSuccess) e = cudaMalloc(&ctx->d_work, sizeof(unsigned long long) * zg::kWorkWords);
+    if (e == cudaSuccess) e = cudaMemset(ctx->d_work, 0, sizeof(unsigned long long) * zg::kWorkWords);
     if (e == cudaSuccess) e = cudaMallocHost(&ctx->h_sc, sizeof(zg::Scalars));
     if (e == cudaSuccess) {
         memset(ctx->h_sc, 0, sizeof(zg::Scalars));
@@ -613,6 +616,7 @@ void zg_destroy(zg_ctx *ctx)
     if (!ctx) return;
     if (ctx->d_sc) cudaFree(ctx->d_sc);
     if (ctx->d_partials) cudaFree(ctx->d_partials);
+    if (ctx->d_work) cudaFree(ctx->d_work);
     if (ctx->h_sc) cudaFreeHost(ctx->h_sc);
     delete ctx;
 }

@@ -15,8 +15,8 @@ namespace zg {
 
 constexpr int kGatherThreads = 256;
 constexpr int kGatherUnroll = 4;    // independent bf16 vectors in flight per thread
-constexpr int kGatherUnrollMx = 2;  // independent MX vectors in flight per thread
-constexpr int kMxVec = 16;        // MX elements per thread per vector: one 16-byte code load
+constexpr int kGatherUnrollMx = 4;  // independent MX vectors in flight per thread
+constexpr int kMxVec = 8;           // MX elements per thread per vector: one 8-byte code load, one 16-byte store
 
 // Owner of flat index i: rank floor(i / s). The binary32 estimate i * (1/s)
 // carries a relative error below 2^-22 and i / s < 16, so it is within 2^-18
@@ -67,21 +67,22 @@ __device__ __forceinline__ uint32_t mx_to_bf16(float x)
     return x != x ? 0x7fc0u : uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(x)));
 }
 
-// 16 codes of one block at one scale byte to 16 bf16 values (8 words, element
+// 8 codes of one block at one scale byte to 8 bf16 values (4 words, element
 // 2k in the low half). A NaN scale or any NaN code (0x7F / 0xFF, which the
 // encoder writes only into blocks with a NaN scale) sends the vector down the
 // element-wise path, which maps NaN to 0x7FC0.
-__device__ __forceinline__ void mx16_to_bf16(uint4 c, uint32_t sbyte, uint32_t (&w)[8])
+__device__ __forceinline__ uint4 mx8_to_bf16(uint2 c, uint32_t sbyte)
 {
-    const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
+    const uint32_t cw[2] = {c.x, c.y};
     uint32_t nan = sbyte == 0xffu;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) nan |= __vcmpeq4(cw[q] & 0x7f7f7f7fu, 0x7f7f7f7fu);
+    for (int q = 0; q < 2; ++q) nan |= __vcmpeq4(cw[q] & 0x7f7f7f7fu, 0x7f7f7f7fu);
     const float scale = e8m0_value(sbyte);
+    uint32_t w[4];
     if (!nan) {
         const float2 s2 = make_float2(scale, scale);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
+        for (int q = 0; q < 2; ++q) {
             const float2 a = mul_f32x2(e4m3x2_to_f32x2(uint16_t(cw[q])), s2);
             const float2 b = mul_f32x2(e4m3x2_to_f32x2(uint16_t(cw[q] >> 16)), s2);
             w[2 * q] = pack_bf16x2(a.x, a.y);
@@ -89,11 +90,12 @@ __device__ __forceinline__ void mx16_to_bf16(uint4 c, uint32_t sbyte, uint32_t (
         }
     } else {
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
+        for (int q = 0; q < 4; ++q) {
             const float2 f = e4m3x2_to_f32x2(uint16_t(cw[q >> 1] >> (16 * (q & 1))));
             w[q] = mx_to_bf16(__fmul_rn(f.x, scale)) | (mx_to_bf16(__fmul_rn(f.y, scale)) << 16);
         }
     }
+    return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
 // The owning shard of the index a thread is at. A thread's indices only grow
@@ -154,9 +156,11 @@ __global__ void __launch_bounds__(kGatherThreads)
     }
 }
 
-// MX shards -> bf16 out[0, n). With lo a multiple of 16 each thread decodes
-// 16 codes of one 32-element block (one 16-byte load, one scale byte) into
-// two 16-byte stores; otherwise element by element.
+// MX shards -> bf16 out[0, n). With lo a multiple of 8 each thread decodes
+// 8 codes of one 32-element block (one 8-byte load, one scale byte shared by
+// four lanes) into one 16-byte store, so a warp's loads and stores each
+// cover one contiguous span (256 and 512 bytes); otherwise element by
+// element.
 __global__ void __launch_bounds__(kGatherThreads)
     gather_mx_kernel(MxShards sh, Owner own, int64_t lo, int64_t n, uint16_t *__restrict__ out)
 {
@@ -169,7 +173,7 @@ __global__ void __launch_bounds__(kGatherThreads)
         const int64_t nvec = n / kMxVec;
 #pragma unroll 1
         for (int64_t v0 = tid; v0 < nvec; v0 += kGatherUnrollMx * stride) {
-            uint4 c[kGatherUnrollMx];
+            uint2 c[kGatherUnrollMx];
             uint32_t sb[kGatherUnrollMx];
 #pragma unroll
             for (int u = 0; u < kGatherUnrollMx; ++u) {
@@ -181,20 +185,14 @@ __global__ void __launch_bounds__(kGatherThreads)
                         sbase = pick(sh.s, cur.r);
                     }
                     const int64_t k = i - cur.start;
-                    c[u] = ld_stream(reinterpret_cast<const uint4 *>(cbase + k));
+                    c[u] = ld_stream(reinterpret_cast<const uint2 *>(cbase + k));
                     sb[u] = sbase[k >> 5];
                 }
             }
 #pragma unroll
             for (int u = 0; u < kGatherUnrollMx; ++u) {
                 const int64_t v = v0 + u * stride;
-                if (v < nvec) {
-                    uint32_t w[8];
-                    mx16_to_bf16(c[u], sb[u], w);
-                    uint4 *o = reinterpret_cast<uint4 *>(out + v * kMxVec);
-                    o[0] = make_uint4(w[0], w[1], w[2], w[3]);
-                    o[1] = make_uint4(w[4], w[5], w[6], w[7]);
-                }
+                if (v < nvec) reinterpret_cast<uint4 *>(out)[v] = mx8_to_bf16(c[u], sb[u]);
             }
         }
         done = nvec * kMxVec;

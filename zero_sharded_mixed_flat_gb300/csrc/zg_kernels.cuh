@@ -79,7 +79,15 @@ struct State {
     uint16_t *p;        // bf16 parameters (written unless MX parameters are bound)
     uint8_t *pcodes;    // MXFP8 parameters: E4M3 codes, one per element, or null
     uint8_t *pscales;   // and their E8M0 scales, one per 32 elements
+    unsigned long long *work;  // the step pass's chunk counters (kWorkWords words, zero between launches)
 };
+
+// The fused step pass hands out its vectors in warp chunks from kWorkLanes
+// counters, each in its own 256-byte line of a small device array that is
+// zero between launches (the last block of a launch clears it).
+constexpr int kWorkLanes = 8;
+constexpr int kWorkStride = 32;  // 64-bit words from one counter to the next
+constexpr int kWorkWords = kWorkLanes * kWorkStride;
 
 constexpr int kStatusTimeout = -5;     // ZG_ERR_DEVICE_TIMEOUT
 constexpr int kStatusStaleNorm = -6;   // ZG_ERR_STALE_NORM
@@ -715,13 +723,17 @@ struct StepMinBlocks<StagedSrc> {
 
 // The last block of a step pass commits the step count (unless skipped) and
 // marks the norm consumed, so a repeated step pass cannot apply twice.
-__device__ __forceinline__ void step_epilogue(Scalars *sc, int skip)
+__device__ __forceinline__ void step_epilogue(Scalars *sc, int skip, unsigned long long *work = nullptr)
 {
     __syncthreads();
     if (threadIdx.x != 0) return;
     __threadfence();
     const unsigned int ticket = atomicAdd(&sc->step_ticket, 1u);
     if (ticket != gridDim.x - 1) return;
+    if (work) {  // every warp has taken its last chunk: clear the counters for the next launch
+#pragma unroll
+        for (int q = 0; q < kWorkLanes; ++q) work[q * kWorkStride] = 0ull;
+    }
     if (skip == 2) {
         sc->status = kStatusStaleNorm;
     } else {
@@ -928,8 +940,58 @@ __device__ __forceinline__ bool step_thread_loop(const Src &src, int64_t n, floa
     return any;
 }
 
+// One warp's share of the fused step pass, split dynamically. The vectors
+// form chunks of 32 * U (U per lane, lane-consecutive); chunk q + 8j belongs
+// to counter q (the warp's index in its block). A warp's first chunk is fixed
+// (j = its block index, so the first wave covers the same vectors a
+// grid-stride split would), the following ones come from its counter
+// (j = grid + the counter's next value), fetched while the current chunk's
+// loads are in flight. Warps whose loads return sooner take more chunks, so
+// the launch ends together: with a fixed grid-stride split the blocks of one
+// launch finished up to 10 us apart at N = 2^24 (GB300, one launch about
+// 95 us), as some SMs get their memory traffic served sooner than others.
+// Every element gets the same arithmetic either way, so the results are
+// bit-identical to the fixed split. Indices are mirrored when ZG_STEP_REVERSE
+// walks from the end. True when the warp stored anything.
+template <class Src>
+__device__ __forceinline__ bool step_chunk_loop(const Src &src, int64_t n, float inv, float c, float bc1, float bc2,
+                                                const StepK &k, const State &st)
+{
+    constexpr int U = StepUnroll<Src>::value;
+    constexpr int64_t kChunk = 32 * U;
+    static_assert(kStepThreads / 32 == kWorkLanes, "one counter per warp of a block");
+    const int64_t nvec = n / kVec;
+    const int64_t nchunk = (nvec + kChunk - 1) / kChunk;
+    const int lane = threadIdx.x & 31;
+    const int q = threadIdx.x >> 5;
+    unsigned long long *ctr = st.work + q * kWorkStride;
+    int64_t ch = q + int64_t(kWorkLanes) * blockIdx.x;
+    bool any = false;
+#pragma unroll 1
+    while (ch < nchunk) {  // warp-uniform
+        unsigned long long next = 0ull;
+        if (lane == 0) next = atomicAdd(ctr, 1ull);
+        VecData<Src> d[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t vv = ch * kChunk + u * 32 + lane;
+            if (vv < nvec) step_load(src, ZG_STEP_REVERSE ? nvec - 1 - vv : vv, st, d[u]);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t vv = ch * kChunk + u * 32 + lane;
+            if (vv < nvec)
+                step_compute_store(src, ZG_STEP_REVERSE ? nvec - 1 - vv : vv, d[u], inv, c, bc1, bc2, k, st);
+        }
+        any = true;
+        next = __shfl_sync(0xffffffffu, next, 0);
+        ch = q + int64_t(kWorkLanes) * (int64_t(gridDim.x) + int64_t(next));
+    }
+    return any;
+}
+
 // Fused reduce-scatter + unscale + clip + AdamW + bf16 all-gather, one pass,
-// plain 128-bit loads and stores, grid-stride over 8-element vectors.
+// plain 128-bit loads and stores over 8-element vectors in warp chunks.
 template <class Src, bool kMxOut = false>
 __global__ void __launch_bounds__(kStepThreads, StepMinBlocks<Src>::value)
     step_kernel(Src src, int64_t n, float inv, StepK k, State st, Scalars *sc)
@@ -975,11 +1037,10 @@ __global__ void __launch_bounds__(kStepThreads, StepMinBlocks<Src>::value)
         }
         if (blockIdx.x == 0 && threadIdx.x == 0) step_tail_mx(src, n, inv, c, bc1, bc2, k, st);
     } else if (skip == 0) {
-        step_thread_loop(src, n, inv, c, bc1, bc2, k, st, int64_t(blockIdx.x) * kStepThreads + threadIdx.x,
-                         int64_t(gridDim.x) * kStepThreads);
+        step_chunk_loop(src, n, inv, c, bc1, bc2, k, st);
         if (blockIdx.x == 0 && threadIdx.x == 0) step_tail(src, n, inv, c, bc1, bc2, k, st);
     }
-    step_epilogue(sc, skip);
+    step_epilogue(sc, skip, kMxOut ? nullptr : st.work);
 }
 
 // ------------------------------------------------------------------ launch
