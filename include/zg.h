@@ -112,8 +112,10 @@ typedef struct {
 
 /* Create a context for N parameters over P simulated ranks (1 <= P <= 16,
  * 1 <= N < 2^62) on the current CUDA device. Allocates only a small device
- * workspace (64 KB of fp64 norm-pass block partials, 2 KB of counters the
- * step pass hands out its work with, and a 112-byte block of step scalars).
+ * workspace (64 KB of fp64 block partials for the MXFP8 and one-launch norm
+ * passes, a 4.5 KB work array with the counters the norm and step passes hand
+ * out their work with and the norm's exact fixed-point sum, and a 112-byte
+ * block of step scalars).
  * Step count starts at 0. Layout: Zero From Scratch, item 17 (one flat
  * vector cut into P contiguous shards). *out is NULL on failure. */
 int zg_init(int64_t n, int p, const zg_hparams *hp, zg_ctx **out);
@@ -137,9 +139,11 @@ int zg_bind(zg_ctx *ctx, float *w, float *m, float *v, uint16_t *params_bf16);
 int zg_step(zg_ctx *ctx, const uint16_t *const *grad_ptrs, float loss_scale, zg_stream stream);
 
 /* First half of a step: the global norm (item 7's reduce-scatter, summed and
- * squared, then one scalar all-reduce, here an ordered sum of block
- * partials), the found-inf decision, the clip factor and the next bias
- * corrections, all left in device memory. Reads 2P bytes per parameter. */
+ * squared, then one scalar all-reduce, here an exact sum of per-chunk
+ * partial sums rounded once to binary64, so the result does not depend on
+ * how the work was spread over the GPU), the found-inf decision, the clip
+ * factor and the next bias corrections, all left in device memory. Reads 2P
+ * bytes per parameter. */
 int zg_grad_norm(zg_ctx *ctx, const uint16_t *const *grad_ptrs, float loss_scale, zg_stream stream);
 
 /* The first half of a step taken bucket by bucket, so each bucket's share of
@@ -334,18 +338,16 @@ int zg_probe_copy(const void *src, void *dst, int64_t bytes, zg_stream stream);
  * grad_average 0 or 1. Other values are rejected with ZG_ERR_INVALID_ARG or
  * ZG_ERR_MISALIGNED and a message in zg_last_error.
  * It allocates nothing: no cudaMalloc, no cudaFree, no allocating library
- * call. Its scratch is a fixed 33,024-byte array inside the library's device
- * image (block partials for at most 4096 blocks, which bounds the launch grid,
- * plus a result block); every GPU that loads the library holds that array
- * until the process exits. The first call on a device looks up the array's
+ * call. Its scratch is a fixed 4,864-byte array inside the library's device
+ * image (a result block and the norm pass's work array); every GPU that loads
+ * the library holds that array until the process exits. The first call on a device looks up the array's
  * device address (cudaGetSymbolAddress), so make that first call before any
  * stream capture; after a device reset (a new CUDA context on the device) the
  * next call looks the address up again, and should likewise come before any
  * capture. Every pointer is checked for the kind of memory behind it, asked
  * of the driver on every call (nothing is remembered). All calls on a device
- * share the array and each clears its result block and counter first: calls
- * that overlap on the GPU race and must be ordered by the caller (one stream,
- * or events). Stream-ordered; does not wait. */
+ * share the array and each clears it first: calls that overlap on the GPU
+ * race and must be ordered by the caller (one stream, or events). Stream-ordered; does not wait. */
 int zg_grad_norm_noalloc(const uint16_t *const *grad_ptrs, int p, int64_t n, float loss_scale, int grad_average,
                          double *out, zg_stream stream);
 

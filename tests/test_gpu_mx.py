@@ -155,7 +155,11 @@ def _lossless_bf16(n: int, seed: int) -> np.ndarray:
 @pytest.mark.parametrize("n,p", [(4099, 4), ((1 << 20) + 96, 8)])
 def test_mx_step_on_lossless_gradients_equals_bf16_step(n, p):
     """Encoded on the GPU, gradients MXFP8 holds exactly must give the MX step
-    the bf16 step's bits (the two decode paths meet on the same fp32 values)."""
+    the bf16 step's bits (the two decode paths meet on the same fp32 values).
+    The two norm passes add the same squares in different orders (the bf16
+    pass exactly over warp chunks, the MX pass over its own fixed grid), so
+    their sums of squares agree to 1e-12; the clip factor (1 here) and the
+    state must be the same bits."""
     w0 = (np.random.default_rng(n).standard_normal(n) * 0.02).astype(np.float32)
     a, b = GpuRun(w0, p), GpuRun(w0, p)
     for t in range(3):
@@ -168,10 +172,31 @@ def test_mx_step_on_lossless_gradients_equals_bf16_step(n, p):
         zb.zg_step(a.ctx, dev, 1024.0)
         zb.zg_step_mxfp8(b.ctx, codes, scales, 1024.0)
         ia, ib = zb.zg_get_info(a.ctx), zb.zg_get_info(b.ctx)
-        assert ia.status == ib.status == 0 and ia.sumsq == ib.sumsq and ia.clip_coef == ib.clip_coef, (t, ia, ib)
+        assert ia.status == ib.status == 0 and ia.clip_coef == ib.clip_coef == 1.0, (t, ia, ib)
+        assert abs(ia.sumsq - ib.sumsq) <= 1e-12 * ib.sumsq, (t, ia, ib)
     sa, sb = a.state(), b.state()
     for k in sa:
         assert sa[k].tobytes() == sb[k].tobytes(), k
+
+
+@pytest.mark.parametrize("n,p", [(1, 1), (7, 2), (4099, 4), (65_549, 8), ((1 << 20) + 13, 8), (300_017, 16)])
+def test_quant_norm_equals_bf16_norm_on_lossless_gradients(n, p):
+    """On gradients MXFP8 holds exactly, the fused encode-and-norm pass forms
+    the bf16 norm pass's g (exact decoded products summed in rank order) and
+    sums its squares the same way (the same warp chunks over g padded to
+    whole vectors, the same butterfly, the same exact total): the same bits,
+    ragged N included."""
+    host = [_lossless_bf16(n, 77 * n + r) for r in range(p)]
+    dev = [to_dev_bf16(h) for h in host]
+    a, b = zb.zg_init(n, p), zb.zg_init(n, p)
+    nb = (n + 31) // 32
+    codes = [torch.empty(n, dtype=torch.uint8, device="cuda") for _ in range(p)]
+    scales = [torch.empty(nb, dtype=torch.uint8, device="cuda") for _ in range(p)]
+    zb.zg_grad_norm(a, dev, 1024.0)
+    zb.zg_quant_norm_mxfp8(b, dev, codes, scales, 1024.0)
+    ia, ib = zb.zg_get_info(a), zb.zg_get_info(b)
+    assert ia.status == ib.status == 0 and not ia.found_inf
+    assert (ia.sumsq, ia.norm, ia.clip_coef) == (ib.sumsq, ib.norm, ib.clip_coef), (n, p, ia, ib)
 
 
 @pytest.mark.parametrize("n,p", [(1, 1), (7, 2), (33, 3), (1000, 8), (65_549, 8), (20_011, 11), (4096, 16),

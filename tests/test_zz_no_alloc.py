@@ -8,8 +8,8 @@ inside the library. These tests call it through the C ABI several times in a
 row, on different sizes and rank counts, so every call runs on whatever the
 previous one left in the shared array, and check each result:
 
-- bit for bit against zg_grad_norm, the entry point that keeps its partials
-  in a cudaMalloc'd workspace (same kernel, same grid, same summation);
+- bit for bit against zg_grad_norm, the entry point that keeps its work
+  array in a cudaMalloc'd workspace (same kernel, same exact summation);
 - against the oracle's sum of squares of the reduced, unscaled gradient,
   within the norm tolerance of the other tests (relative 1e-5);
 - on the degenerate sizes N = 1 and 7 and a ragged N = 65,549;

@@ -35,7 +35,7 @@ struct zg_ctx {
     zg::Scalars *d_sc;
     double *d_partials;
     int partials_cap;
-    unsigned long long *d_work;  // the step pass's chunk counters (zg::kWorkWords words)
+    unsigned long long *d_work;  // the step and norm passes' work array (zg::kWorkWords words)
     zg::Scalars *h_sc;
     int variant;
     long long wait_limit;
@@ -365,8 +365,8 @@ int zg_grad_norm(zg_ctx *ctx, const uint16_t *const *grad_ptrs, float loss_scale
     if (int rc = check_ctx(ctx, false)) return rc;
     if (int rc = check_scale(loss_scale)) return rc;
     if (int rc = check_rank_ptrs(ctx, grad_ptrs, "grad_ptrs", true)) return rc;
-    return finish_launch(zg::launch_norm_bf16(ctx->p, grad_ptrs, ctx->n, inv_scale(ctx, loss_scale), ctx->d_partials,
-                                              ctx->partials_cap, ctx->d_sc, ctx->fk, stream,
+    return finish_launch(zg::launch_norm_bf16(ctx->p, grad_ptrs, ctx->n, inv_scale(ctx, loss_scale), ctx->d_work,
+                                              ctx->d_sc, ctx->fk, stream,
                                               ctx->variant == ZG_VARIANT_STAGED ? ctx->stage : nullptr),
                          "norm pass launch");
 }
@@ -399,8 +399,8 @@ int zg_grad_norm_bucket(zg_ctx *ctx, const uint16_t *const *grad_ptrs, int64_t l
     float *stage = ctx->variant == ZG_VARIANT_STAGED ? ctx->stage + lo : nullptr;
     const int mode = zg::kNormBucket | ((flags & ZG_BUCKET_FIRST) ? zg::kNormFirst : 0) |
                      ((flags & ZG_BUCKET_LAST) ? zg::kNormLast : 0);
-    const int rc = finish_launch(zg::launch_norm_bf16(ctx->p, g, hi - lo, inv_scale(ctx, loss_scale), ctx->d_partials,
-                                                      ctx->partials_cap, ctx->d_sc, ctx->fk, stream, stage, mode),
+    const int rc = finish_launch(zg::launch_norm_bf16(ctx->p, g, hi - lo, inv_scale(ctx, loss_scale), ctx->d_work,
+                                                      ctx->d_sc, ctx->fk, stream, stage, mode),
                                  "bucket norm launch");
     if (rc == ZG_OK) {
         ctx->bucket_open = !(flags & ZG_BUCKET_LAST);
@@ -475,7 +475,7 @@ int zg_quant_norm_mxfp8(zg_ctx *ctx, const uint16_t *const *grad_ptrs, uint8_t *
     if (int rc = check_rank_ptrs(ctx, codes, "codes", true)) return rc;
     if (int rc = check_rank_ptrs(ctx, scales, "scales", false)) return rc;
     return finish_launch(zg::launch_quant_norm(ctx->p, grad_ptrs, codes, scales, ctx->n, inv_scale(ctx, loss_scale),
-                                               ctx->d_partials, ctx->partials_cap, ctx->d_sc, ctx->fk, stream,
+                                               ctx->d_work, ctx->d_sc, ctx->fk, stream,
                                                ctx->variant == ZG_VARIANT_STAGED ? ctx->stage : nullptr),
                          "MX encode and norm pass launch");
 }

@@ -79,15 +79,23 @@ struct State {
     uint16_t *p;        // bf16 parameters (written unless MX parameters are bound)
     uint8_t *pcodes;    // MXFP8 parameters: E4M3 codes, one per element, or null
     uint8_t *pscales;   // and their E8M0 scales, one per 32 elements
-    unsigned long long *work;  // the step pass's chunk counters (kWorkWords words, zero between launches)
+    unsigned long long *work;  // the work array below (kWorkWords words, zero between launches)
 };
 
-// The fused step pass hands out its vectors in warp chunks from kWorkLanes
-// counters, each in its own 256-byte line of a small device array that is
-// zero between launches (the last block of a launch clears it).
+// The work array, a small device array that is zero between launches (the
+// last block of each launch clears what it used). The fused step pass and the
+// norm pass each hand out their vectors in warp chunks from kWorkLanes
+// counters, each counter in its own 256-byte line; the norm pass also adds
+// its exact sum of squares into kAccDigits words and records non-finite
+// squares in one flag word.
 constexpr int kWorkLanes = 8;
 constexpr int kWorkStride = 32;  // 64-bit words from one counter to the next
-constexpr int kWorkWords = kWorkLanes * kWorkStride;
+constexpr int kStepCtr = 0;                              // the step pass's counters
+constexpr int kNormCtr = kStepCtr + kWorkLanes * kWorkStride;  // the norm pass's counters
+constexpr int kAccDigits = 12;                           // base-2^32 digits of the norm's fixed-point sum
+constexpr int kNormAcc = kNormCtr + kWorkLanes * kWorkStride;
+constexpr int kNormFlags = kNormAcc + 16;                // bit 0: an infinite square, bit 1: a NaN one
+constexpr int kWorkWords = kNormFlags + kWorkStride;
 
 constexpr int kStatusTimeout = -5;     // ZG_ERR_DEVICE_TIMEOUT
 constexpr int kStatusStaleNorm = -6;   // ZG_ERR_STALE_NORM
@@ -521,26 +529,29 @@ constexpr int kNormFlush = 4;  // vectors (32 elements) per two-sum run before w
 constexpr int64_t kStageKeepBytes = int64_t(ZG_STAGE_KEEP_MB) << 20;
 static_assert(kNormFlush % kNormUnroll == 0, "a run holds whole unrolled groups");
 
-// Finalize: runs once, in the last block of the norm pass (thread 0).
-__device__ __forceinline__ void finalize_decision(Scalars *sc, double sumsq, const FinalizeK &fk)
+// Finalize: runs once, in the last block of the norm pass (thread 0), given
+// the step count and running powers the step passes left in `sc`.
+__device__ __forceinline__ void finalize_decision(Scalars *sc, double sumsq, const FinalizeK &fk, int64_t t,
+                                                  double b1p, double b2p)
 {
     const int bad = !isfinite(sumsq);
     sc->sumsq = sumsq;
     sc->norm = sqrt(sumsq);
     sc->found_inf = bad;
     if (bad) {
-        sc->t_next = sc->t;
-        sc->b1p_next = sc->b1p;
-        sc->b2p_next = sc->b2p;
+        sc->t_next = t;
+        sc->b1p_next = b1p;
+        sc->b2p_next = b2p;
         sc->clip = 1.0f;
         sc->bc1 = 1.0f;
         sc->bc2 = 1.0f;
     } else {
-        sc->t_next = sc->t + 1;
-        sc->b1p_next = sc->b1p * fk.beta1;
-        sc->b2p_next = sc->b2p * fk.beta2;
-        sc->bc1 = float(1.0 - sc->b1p_next);
-        sc->bc2 = float(1.0 - sc->b2p_next);
+        const double b1n = b1p * fk.beta1, b2n = b2p * fk.beta2;
+        sc->t_next = t + 1;
+        sc->b1p_next = b1n;
+        sc->b2p_next = b2n;
+        sc->bc1 = float(1.0 - b1n);
+        sc->bc2 = float(1.0 - b2n);
         if (fk.max_grad_norm > 0.0) {
             const double q = fk.max_grad_norm / (sc->norm + fk.norm_eps);
             sc->clip = float(q < 1.0 ? q : 1.0);
@@ -549,6 +560,11 @@ __device__ __forceinline__ void finalize_decision(Scalars *sc, double sumsq, con
         }
     }
     sc->norm_gen = sc->norm_gen + 1u;
+}
+
+__device__ __forceinline__ void finalize_decision(Scalars *sc, double sumsq, const FinalizeK &fk)
+{
+    finalize_decision(sc, sumsq, fk, sc->t, sc->b1p, sc->b2p);
 }
 
 // The end of every norm pass: the block's fixed-tree sum of the threads'
@@ -663,22 +679,267 @@ __device__ __forceinline__ double norm_thread_sum(const Src &src, int64_t n, flo
     return acc;
 }
 
-// Grid-stride over 8-element vectors. Each thread owns a fixed set of
-// vectors (a function of N and the grid only), squares g in fp32, adds runs
-// of 32 squares with two-sum and widens each run to fp64; blocks reduce in a
-// fixed tree and the last block to finish sums the block partials in index
-// order. Same N, P and grid: bit-identical norm, run after run.
+// ------------------------------------------------------------------ exact, order-free norm sum
+//
+// The norm pass hands out its vectors in warp chunks, like the step pass, so
+// which warp sums which chunk changes from launch to launch; the norm must
+// not. A chunk is 32 consecutive vectors (one per lane): each lane adds its
+// eight squares with two-sum into a binary32 pair (hi, lo), and the warp
+// combines the 32 pairs in a fixed butterfly of pair additions (two-sum of
+// the high parts, the low parts and the error added, renormalised), which
+// leaves the chunk's sum as one pair (H, L) in every lane. H and L are
+// binary32 values, integer multiples of 2^-149, and are added EXACTLY into a
+// fixed-point accumulator that counts units of 2^-149 in kAccDigits base-2^32
+// digits held one per lane (a 64-bit word per digit, so signed contributions
+// and carries wait until the end). Integer addition does not care about
+// order: the total is the exact sum of the chunk pairs, the same whichever
+// warps took the chunks and whatever the grid. A chunk whose pair is not
+// finite (a square that is inf or NaN, or a binary32 sum that overflowed)
+// adds its finite squares one by one, exactly, and flags the others. The
+// chunks are defined on g padded with zeros to whole vectors, so any pass
+// that forms the same g (the fused MX encode-and-norm pass from decoded
+// codes, when those hold the gradients exactly) gets the same bits.
+// Blocks add their warps' words into the work array; the last block to
+// finish turns the words into the correctly rounded binary64 sum of squares
+// (non-finite when a square was: NaN before inf) and makes the decision.
+
+__device__ __forceinline__ void two_sum(float a, float b, float &s, float &e)
+{
+    s = __fadd_rn(a, b);
+    const float bp = __fsub_rn(s, a);
+    e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bp)), __fsub_rn(b, bp));
+}
+
+// (h, l) + (oh, ol) as binary32 pairs; the same bits whichever operand comes
+// first (two-sum's error term is exact, and each addition is commutative).
+__device__ __forceinline__ void pair_add(float &h, float &l, float oh, float ol)
+{
+    float s, e;
+    two_sum(h, oh, s, e);
+    const float t = __fadd_rn(__fadd_rn(l, ol), e);
+    h = __fadd_rn(s, t);
+    l = __fsub_rn(t, __fsub_rn(h, s));
+}
+
+// Adds x * 2^149 (x a finite binary32 value of either sign, so an integer) to
+// the digits held one per lane: x = m * 2^(max(E, 1) - 150) for the biased
+// exponent E and the significand m, so x * 2^149 = m << (max(E, 1) - 1),
+// which touches two digits.
+__device__ __forceinline__ void acc_add(long long &word, float x, int lane)
+{
+    const uint32_t b = __float_as_uint(x);
+    const uint32_t e = (b >> 23) & 0xffu;
+    const uint32_t sh = (e ? e : 1u) - 1u;
+    const uint64_t v = uint64_t((b & 0x7fffffu) | (e ? 0x800000u : 0u)) << (sh & 31u);
+    const int k = int(sh >> 5);
+    const long long add = lane == k ? (long long)(v & 0xffffffffull) : (lane == k + 1 ? (long long)(v >> 32) : 0ll);
+    word += (b >> 31) ? -add : add;
+}
+
+// The accumulated digits as the correctly rounded binary64 value of their
+// sum times 2^-149 (the sum is non-negative). One thread.
+__device__ __forceinline__ double acc_to_double(const long long (&w)[kAccDigits])
+{
+    uint32_t d[kAccDigits];
+    long long carry = 0;
+#pragma unroll
+    for (int i = 0; i < kAccDigits; ++i) {
+        const long long t = w[i] + carry;
+        d[i] = uint32_t(t);
+        carry = t >> 32;  // floor division by 2^32
+    }
+    int top = -1;
+#pragma unroll
+    for (int i = 0; i < kAccDigits; ++i)
+        if (d[i] != 0u) top = i;
+    if (top < 0) return 0.0;
+    // the 96 bits from the top digit down, shifted to put the leading one at
+    // bit 95; the high 64 of them, with every lower bit folded into a sticky
+    // bit 0 (below the rounding position), round as the whole would
+    uint32_t a = 0u, b = 0u, c = 0u;
+    bool sticky = false;
+#pragma unroll
+    for (int i = 0; i < kAccDigits; ++i) {  // constant indices: the digits stay in registers
+        a = i == top ? d[i] : a;
+        b = i == top - 1 ? d[i] : b;
+        c = i == top - 2 ? d[i] : c;
+        sticky |= i < top - 2 && d[i] != 0u;
+    }
+    const int lz = __clz(a);
+    const uint64_t ab = (uint64_t(a) << 32) | b;
+    uint64_t y = lz ? (ab << lz) | (uint64_t(c) >> (32 - lz)) : ab;
+    const uint32_t rest = lz ? (c << lz) : c;
+    if (rest != 0u || sticky) y |= 1ull;
+    const int k = 32 * (top - 1) - lz - 149;  // y * 2^k, with -212 <= k <= 171
+    return __ull2double_rn(y) * __longlong_as_double((long long)(k + 1023) << 52);
+}
+
+// One chunk's contribution: each lane holds its vector's eight g values and
+// the two-sum pair (hi, lo) of their squares in element order. The warp's
+// 32 pairs are combined by a fixed butterfly (xor distances 16, 8, 4, 2, 1)
+// into the chunk pair, added exactly to the digits; if a lane's pair or the
+// chunk pair is not finite, every square is added on its own instead and
+// the non-finite ones are flagged. Warp-uniform; every lane must take part.
+__device__ __forceinline__ void chunk_add(float hi, float lo, const float (&g)[kVec], int lane, long long &word,
+                                          uint32_t &flags)
+{
+    if (__all_sync(0xffffffffu, isfinite(hi) && isfinite(lo))) {
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1)
+            pair_add(hi, lo, __shfl_xor_sync(0xffffffffu, hi, off), __shfl_xor_sync(0xffffffffu, lo, off));
+        if (isfinite(hi) && isfinite(lo)) {  // the same in every lane
+            acc_add(word, hi, lane);
+            acc_add(word, lo, lane);
+            return;
+        }
+    }
+    // rare: every square on its own, broadcast from its lane
+#pragma unroll 1
+    for (int from = 0; from < 32; ++from) {
+#pragma unroll
+        for (int j = 0; j < kVec; ++j) {
+            const float x = __shfl_sync(0xffffffffu, __fmul_rn(g[j], g[j]), from);
+            if (isfinite(x))
+                acc_add(word, x, lane);
+            else
+                flags |= isnan(x) ? 2u : 1u;
+        }
+    }
+}
+
+// One warp's share of the norm pass over warp chunks (see above), adding
+// into this lane's digit `word` and non-finite flags. The vectors are those
+// of g padded with zeros to a multiple of 8 elements: the last, partial one
+// is read element by element.
+template <class Src, bool kStage>
+__device__ __forceinline__ void norm_chunk_loop(const Src &src, int64_t n, float inv, float *__restrict__ stage,
+                                                unsigned long long *work, long long &word, uint32_t &flags)
+{
+    const int64_t nfull = n / kVec;
+    const int64_t nvec = (n + kVec - 1) / kVec;
+    const int64_t nchunk = (nvec + 31) / 32;
+    const int lane = threadIdx.x & 31;
+    const int q = threadIdx.x >> 5;
+    unsigned long long *ctr = work + kNormCtr + q * kWorkStride;
+    int64_t ch = q + int64_t(kWorkLanes) * blockIdx.x;
+#pragma unroll 1
+    while (ch < nchunk) {  // warp-uniform
+        unsigned long long next = 0ull;
+        if (lane == 0) next = atomicAdd(ctr, 1ull);
+        const int64_t v = ch * 32 + lane;
+        float gh[kVec];
+        float hi = 0.0f, lo = 0.0f;
+        if (v < nfull) {
+            typename Src::Raw raw;
+            src.load_norm(v, raw);
+            src.reduce(raw, gh);
+        } else {
+#pragma unroll
+            for (int j = 0; j < kVec; ++j) gh[j] = v * kVec + j < n ? src.sum1(v * kVec + j) : 0.0f;
+        }
+#pragma unroll
+        for (int j = 0; j < kVec; ++j) {
+            gh[j] = __fmul_rn(gh[j], inv);
+            two_sum_acc(hi, lo, __fmul_rn(gh[j], gh[j]));
+        }
+        if (kStage && v < nfull) {
+            // keep the reduce-scatter output for the step pass. Its last
+            // kStageKeepBytes (the part the step pass, walking from the end,
+            // reads first) get the default store policy so they can still be
+            // in L2; the rest streams out.
+            float4 *o = reinterpret_cast<float4 *>(stage) + 2 * v;
+            const float4 a = make_float4(gh[0], gh[1], gh[2], gh[3]);
+            const float4 b = make_float4(gh[4], gh[5], gh[6], gh[7]);
+            if (v >= nfull - kStageKeepBytes / 32) {
+                o[0] = a;
+                o[1] = b;
+            } else {
+                __stcs(o, a);
+                __stcs(o + 1, b);
+            }
+        } else if (kStage && v < nvec) {
+#pragma unroll
+            for (int j = 0; j < kVec; ++j)
+                if (v * kVec + j < n) stage[v * kVec + j] = gh[j];
+        }
+        chunk_add(hi, lo, gh, lane, word, flags);
+        next = __shfl_sync(0xffffffffu, next, 0);
+        ch = q + int64_t(kWorkLanes) * (int64_t(gridDim.x) + int64_t(next));
+    }
+}
+
+// The end of the norm pass: the block's digits and flags go into the work
+// array; the last block to finish (an atomic ticket) takes the words (and
+// clears them, the flags and the norm counters for the next launch), rounds
+// the sum to binary64 and writes the decision (or, for a bucket, adds to the
+// running bucket sum).
+__device__ __forceinline__ void norm_exact_finish(long long word, uint32_t flags, unsigned long long *work,
+                                                  Scalars *sc, const FinalizeK &fk, int mode)
+{
+    __shared__ long long s_acc[kNormThreads / 32][kAccDigits];
+    __shared__ uint32_t s_flags;
+    __shared__ int am_last;
+    const int lane = threadIdx.x & 31, q = threadIdx.x >> 5;
+    if (threadIdx.x == 0) s_flags = 0u;
+    __syncthreads();
+    if (lane < kAccDigits) s_acc[q][lane] = word;
+    if (lane == 0 && flags) atomicOr(&s_flags, flags);
+    __syncthreads();
+    if (threadIdx.x < kAccDigits) {
+        long long t = 0;
+#pragma unroll
+        for (int w = 0; w < kNormThreads / 32; ++w) t += s_acc[w][threadIdx.x];
+        if (t) atomicAdd(work + kNormAcc + threadIdx.x, (unsigned long long)t);
+    } else if (threadIdx.x == kAccDigits && s_flags) {
+        atomicOr(reinterpret_cast<unsigned int *>(work + kNormFlags), s_flags);
+    }
+    if (threadIdx.x <= kAccDigits) __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const unsigned int ticket = atomicAdd(&sc->norm_ticket, 1u);
+        am_last = (ticket == gridDim.x - 1);
+    }
+    __syncthreads();
+    if (!am_last || threadIdx.x != 0) return;
+    __threadfence();
+    // what the decision needs besides the sum, read while the words are fetched
+    const int64_t t = sc->t;
+    const double b1p = sc->b1p, b2p = sc->b2p, bucket_acc = sc->bucket_acc;
+    long long w[kAccDigits];
+#pragma unroll
+    for (int i = 0; i < kAccDigits; ++i) w[i] = (long long)atomicExch(work + kNormAcc + i, 0ull);
+    const unsigned int fl = atomicExch(reinterpret_cast<unsigned int *>(work + kNormFlags), 0u);
+#pragma unroll
+    for (int i = 0; i < kWorkLanes; ++i) work[kNormCtr + i * kWorkStride] = 0ull;
+    double total = acc_to_double(w);
+    if (fl & 2u)
+        total = __longlong_as_double(0x7ff8000000000000ll);  // NaN
+    else if (fl & 1u)
+        total = __longlong_as_double(0x7ff0000000000000ll);  // +inf
+    if (!(mode & kNormBucket)) {
+        finalize_decision(sc, total, fk, t, b1p, b2p);
+    } else {
+        const double run = (mode & kNormFirst) ? total : bucket_acc + total;
+        sc->bucket_acc = run;
+        if (mode & kNormLast) finalize_decision(sc, run, fk, t, b1p, b2p);
+    }
+    sc->norm_ticket = 0u;
+}
+
+// The norm pass: warp chunks, the exact sum above. Same gradients, N and P:
+// bit-identical norm, run after run and on any grid.
 template <class Src, bool kStage = false>
 __global__ void __launch_bounds__(kNormThreads, NormMinBlocks<Src>::value)
-    norm_kernel(Src src, int64_t n, float inv, double *__restrict__ partials, Scalars *sc, FinalizeK fk,
+    norm_kernel(Src src, int64_t n, float inv, unsigned long long *work, Scalars *sc, FinalizeK fk,
                 float *__restrict__ stage = nullptr, int mode = kNormWhole)
 {
+    static_assert(kNormThreads / 32 == kWorkLanes && kAccDigits <= 32, "one counter per warp, one digit per lane");
     pdl_wait();     // the gradients may come from the kernel just before
     pdl_trigger();  // the step pass may start its blocks as ours retire
-    const double acc = norm_thread_sum<Src, kStage>(src, n, inv, stage,
-                                                    int64_t(blockIdx.x) * kNormThreads + threadIdx.x,
-                                                    int64_t(gridDim.x) * kNormThreads);
-    norm_finish(acc, partials, sc, fk, mode);
+    long long word = 0;
+    uint32_t flags = 0u;
+    norm_chunk_loop<Src, kStage>(src, n, inv, stage, work, word, flags);
+    norm_exact_finish(word, flags, work, sc, fk, mode);
 }
 
 // ------------------------------------------------------------------ fused step pass
@@ -732,7 +993,7 @@ __device__ __forceinline__ void step_epilogue(Scalars *sc, int skip, unsigned lo
     if (ticket != gridDim.x - 1) return;
     if (work) {  // every warp has taken its last chunk: clear the counters for the next launch
 #pragma unroll
-        for (int q = 0; q < kWorkLanes; ++q) work[q * kWorkStride] = 0ull;
+        for (int q = 0; q < kWorkLanes; ++q) work[kStepCtr + q * kWorkStride] = 0ull;
     }
     if (skip == 2) {
         sc->status = kStatusStaleNorm;
@@ -964,7 +1225,7 @@ __device__ __forceinline__ bool step_chunk_loop(const Src &src, int64_t n, float
     const int64_t nchunk = (nvec + kChunk - 1) / kChunk;
     const int lane = threadIdx.x & 31;
     const int q = threadIdx.x >> 5;
-    unsigned long long *ctr = st.work + q * kWorkStride;
+    unsigned long long *ctr = st.work + kStepCtr + q * kWorkStride;
     int64_t ch = q + int64_t(kWorkLanes) * blockIdx.x;
     bool any = false;
 #pragma unroll 1

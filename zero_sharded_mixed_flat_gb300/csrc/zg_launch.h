@@ -13,8 +13,8 @@ namespace zg {
 int wave_blocks(const void *kernel, int threads, size_t smem);
 
 // With `stage` non-null the pass also writes the unscaled fp32 gradient there.
-cudaError_t launch_norm_bf16(int p, const uint16_t *const *g, int64_t n, float inv, double *partials,
-                             int max_blocks, Scalars *sc, FinalizeK fk, cudaStream_t st, float *stage = nullptr,
+cudaError_t launch_norm_bf16(int p, const uint16_t *const *g, int64_t n, float inv, unsigned long long *work,
+                             Scalars *sc, FinalizeK fk, cudaStream_t st, float *stage = nullptr,
                              int mode = kNormWhole);
 // With `stage` non-null the pass also writes the unscaled fp32 gradient there.
 cudaError_t launch_norm_mx(int p, const uint8_t *const *c, const uint8_t *const *s, int64_t n, float inv,
@@ -23,7 +23,7 @@ cudaError_t launch_norm_mx(int p, const uint8_t *const *c, const uint8_t *const 
 // Encode every rank's bf16 gradient to MXFP8 (codes, scales) and take the
 // norm pass from the decoded values, in one launch.
 cudaError_t launch_quant_norm(int p, const uint16_t *const *g, uint8_t *const *codes, uint8_t *const *scales,
-                              int64_t n, float inv, double *partials, int max_blocks, Scalars *sc, FinalizeK fk,
+                              int64_t n, float inv, unsigned long long *work, Scalars *sc, FinalizeK fk,
                               cudaStream_t st, float *stage = nullptr);
 cudaError_t launch_step_bf16(int p, const uint16_t *const *g, int64_t n, float inv, StepK k, State state,
                              Scalars *sc, cudaStream_t st);

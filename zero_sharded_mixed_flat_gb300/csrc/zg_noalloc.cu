@@ -1,7 +1,8 @@
 // zg_noalloc.cu -- the norm pass for callers that cannot allocate device memory.
 //
-// zg_grad_norm keeps its block partials and result in a workspace that
-// zg_init allocates with cudaMalloc. Some callers cannot do that: a process
+// zg_grad_norm keeps its work array (chunk counters and the exact sum of
+// squares) and its result in a workspace that zg_init allocates with
+// cudaMalloc. Some callers cannot do that: a process
 // whose framework allocator has already reserved nearly all device memory
 // (a raw cudaMalloc then fails, or fragments memory the allocator counts on),
 // a latency-critical loop that cannot afford the device synchronisation a
@@ -11,11 +12,12 @@
 // library, so it allocates nothing: the caller passes the gradients and a
 // 16-byte result buffer, and the library touches no other memory.
 //
-// The array (kScratchBytes, about 33 KB) is part of the library's device
+// The array (kScratchBytes, under 5 KB) is part of the library's device
 // image: every GPU that loads the library holds it until the process exits.
-// Every call on a device shares it and it keeps the last call's contents, so
-// each call clears the part that must start at zero (the result block and the
-// block counter) on its stream before launching. Calls that overlap on the
+// Every call on a device shares it. Each call clears it on its stream before
+// launching (the result block, the block counter and the work array must
+// start at zero; a completed launch leaves them so, but an earlier call that
+// did not complete might not have). Calls that overlap on the
 // GPU (on different streams, or from different threads without ordering)
 // race on the array and give wrong results.
 //
@@ -39,10 +41,9 @@
 
 namespace {
 
-constexpr int kNoAllocBlocks = 4096;  // block partials the scratch holds; launches never use more
-constexpr size_t kResultBytes = 256;  // the scalar block (result + counter), padded to keep partials aligned
-constexpr size_t kScratchBytes = kResultBytes + kNoAllocBlocks * sizeof(double);  // 33,024 bytes
-static_assert(sizeof(zg::Scalars) <= kResultBytes, "the scalar block must fit in front of the partials");
+constexpr size_t kResultBytes = 256;  // the scalar block (result + counter), padded to keep the work array aligned
+constexpr size_t kScratchBytes = kResultBytes + zg::kWorkWords * sizeof(unsigned long long);  // 4,864 bytes
+static_assert(sizeof(zg::Scalars) <= kResultBytes, "the scalar block must fit in front of the work array");
 static_assert(offsetof(zg::Scalars, sumsq) == 0 && offsetof(zg::Scalars, norm) == sizeof(double),
               "the result copy takes sumsq and norm as the first 16 bytes");
 
@@ -173,7 +174,7 @@ extern "C" int zg_grad_norm_noalloc(const uint16_t *const *grad_ptrs, int p, int
         return bad(ZG_ERR_CUDA, msg);
     }
     zg::Scalars *sc = static_cast<zg::Scalars *>(scratch);
-    double *partials = reinterpret_cast<double *>(static_cast<unsigned char *>(scratch) + kResultBytes);
+    auto *work = reinterpret_cast<unsigned long long *>(static_cast<unsigned char *>(scratch) + kResultBytes);
     const float inv = float(1.0 / (double(loss_scale) * (grad_average ? double(p) : 1.0)));
     const zg::FinalizeK fk{0.9, 0.999, 0.0, 0.0};  // clip off; only sumsq and norm are returned
 
@@ -182,15 +183,17 @@ extern "C" int zg_grad_norm_noalloc(const uint16_t *const *grad_ptrs, int p, int
         int wave = 0;
         cudaError_t err = wave_of<P>(dev, &wave);
         if (err != cudaSuccess) return err;
-        const int64_t want = (n / zg::kVec + zg::kNormThreads - 1) / zg::kNormThreads;
+        // warp chunks of 32 vectors: no more blocks than give every warp one,
+        // no more than one wave (the sum does not depend on the grid)
+        const int64_t chunks = (n / zg::kVec + 31) / 32;
+        const int64_t want = (chunks + zg::kNormThreads / 32 - 1) / (zg::kNormThreads / 32);
         int64_t blocks = want < 1 ? 1 : want;
         if (blocks > wave) blocks = wave;
-        if (blocks > kNoAllocBlocks) blocks = kNoAllocBlocks;  // the scratch bounds the grid, not N
         zg::Bf16Src<P> src;
         for (int r = 0; r < P; ++r) src.g[r] = grad_ptrs[r];
-        err = cudaMemsetAsync(sc, 0, kResultBytes, stream);  // result block and block counter start at zero
+        err = cudaMemsetAsync(scratch, 0, kScratchBytes, stream);  // result block, counter and work array start at zero
         if (err != cudaSuccess) return err;
-        zg::norm_kernel<zg::Bf16Src<P>><<<int(blocks), zg::kNormThreads, 0, stream>>>(src, n, inv, partials, sc, fk);
+        zg::norm_kernel<zg::Bf16Src<P>><<<int(blocks), zg::kNormThreads, 0, stream>>>(src, n, inv, work, sc, fk);
         err = cudaGetLastError();
         if (err != cudaSuccess) return err;
         return cudaMemcpyAsync(out, sc, 2 * sizeof(double), cudaMemcpyDeviceToDevice, stream);

@@ -3,19 +3,30 @@
 
 namespace zg {
 
-cudaError_t launch_norm_bf16(int p, const uint16_t *const *g, int64_t n, float inv, double *partials,
-                             int max_blocks, Scalars *sc, FinalizeK fk, cudaStream_t st, float *stage, int mode)
+namespace {
+
+// Warp chunks of 32 vectors, one per warp to start with: no more blocks than
+// give every warp a chunk, and no more than one wave.
+int grid_for(const void *kernel, int64_t n)
+{
+    const int64_t chunks = (n / kVec + 31) / 32;
+    const int64_t want = (chunks + kNormThreads / 32 - 1) / (kNormThreads / 32);
+    const int wave = wave_blocks(kernel, kNormThreads, 0);
+    return int(want < 1 ? 1 : (want < wave ? want : wave));
+}
+
+}  // namespace
+
+cudaError_t launch_norm_bf16(int p, const uint16_t *const *g, int64_t n, float inv, unsigned long long *work,
+                             Scalars *sc, FinalizeK fk, cudaStream_t st, float *stage, int mode)
 {
     return with_ranks(p, [&](auto rk) {
         constexpr int P = decltype(rk)::value;
         Bf16Src<P> src;
         for (int r = 0; r < P; ++r) src.g[r] = g[r];
         auto *kernel = stage ? &norm_kernel<Bf16Src<P>, true> : &norm_kernel<Bf16Src<P>, false>;
-        const int64_t want = (n / kVec + kNormThreads - 1) / kNormThreads;
-        int blocks = int(want < 1 ? 1 : (want < max_blocks ? want : max_blocks));
-        const int wave = wave_blocks(reinterpret_cast<const void *>(kernel), kNormThreads, 0);
-        if (blocks > wave) blocks = wave;
-        return launch_dependent(kernel, blocks, kNormThreads, 0, st, src, n, inv, partials, sc, fk, stage, mode);
+        const int blocks = grid_for(reinterpret_cast<const void *>(kernel), n);
+        return launch_dependent(kernel, blocks, kNormThreads, 0, st, src, n, inv, work, sc, fk, stage, mode);
     });
 }
 

@@ -10,22 +10,24 @@
 // and the MX step pass sum them from the payload (packed fused multiply-adds,
 // exact because each product E4M3 * 2^(s - 127) is, and the encoder never
 // writes a scale byte in 247..254). The unscaled, averaged g is squared in
-// fp32 and added with two-sum in runs of four vectors (32 squares) widened to
-// fp64. This saves the P * (1 + 1/32) bytes per parameter the separate norm
-// pass reads back, and P + 1 launches become one.
+// fp32 and summed as the bf16 norm pass sums it: warp chunks of 32 vectors
+// handed out by counters, each lane's two-sum pair, the chunk's fixed
+// butterfly and the exact fixed-point total (so on gradients MXFP8 holds
+// exactly, the two passes give the same bits). This saves the
+// P * (1 + 1/32) bytes per parameter the separate norm pass reads back, and
+// P + 1 launches become one.
 //
 // Each thread issues all P ranks' 16-byte loads of its vector before encoding
 // any (P * 16 bytes in flight per thread, four 256-thread blocks per SM up to
-// P = 8). Work is split in warp-wide rows of 32 consecutive vectors (a block's
-// four quarters sit in neighbouring lanes); the last, partial vector is read
-// and written element by element with the values past N taken as zero, as
-// the encoder takes them.
+// P = 8). A chunk's 32 vectors sit one per lane, so a 32-element block's four
+// quarters are in neighbouring lanes; the last, partial vector is read and
+// written element by element with the values past N taken as zero, as the
+// encoder takes them.
 #include "zg_launch.h"
 
 namespace zg {
 
-constexpr int kQnVec = 8;     // elements per thread per vector: one 16-byte bf16 load per rank
-constexpr int kQnRun = 4;     // vectors per two-sum run (32 squares)
+constexpr int kQnVec = 8;  // elements per thread per vector: one 16-byte bf16 load per rank
 
 template <int P>
 struct QuantNormMinBlocks {
@@ -39,133 +41,110 @@ struct MxOut {
 
 template <int P, bool kStage>
 __global__ void __launch_bounds__(kNormThreads, QuantNormMinBlocks<P>::value)
-    quant_norm_kernel(Bf16Src<P> src, MxOut out, int64_t n, float inv, double *__restrict__ partials, Scalars *sc,
+    quant_norm_kernel(Bf16Src<P> src, MxOut out, int64_t n, float inv, unsigned long long *work, Scalars *sc,
                       FinalizeK fk, float *__restrict__ stage)
 {
+    static_assert(kQnVec == kVec, "the norm pass's chunks are 32 vectors of 8");
     pdl_wait();
     pdl_trigger();
     const int64_t nvec_full = n / kQnVec;
     const int64_t nvec_all = (n + kQnVec - 1) / kQnVec;
-    const int64_t stride = int64_t(gridDim.x) * kNormThreads;
+    const int64_t nchunk = (nvec_all + 31) / 32;
     const int lane = threadIdx.x & 31;
+    const int wq = threadIdx.x >> 5;
     const float2 inv2 = make_float2(inv, inv);
-    double acc = 0.0;
+    unsigned long long *ctr = work + kNormCtr + wq * kWorkStride;
+    int64_t ch = wq + int64_t(kWorkLanes) * blockIdx.x;
+    long long word = 0;
+    uint32_t flags = 0u;
 #pragma unroll 1
-    for (int64_t row = int64_t(blockIdx.x) * kNormThreads + (threadIdx.x & ~31); row < nvec_all;
-         row += kQnRun * stride) {
-        float hi = 0.0f, lo = 0.0f;
-#pragma unroll 1
-        for (int k = 0; k < kQnRun; ++k) {
-            const int64_t base = row + k * stride;
-            if (base >= nvec_all) break;  // warp-uniform
-            const int64_t v = base + lane;
-            // every rank's values of this vector, loads issued together
-            uint32_t wd[P][4];
-            if (v < nvec_full) {
+    while (ch < nchunk) {  // warp-uniform: a chunk is 32 vectors, one per lane
+        unsigned long long next = 0ull;
+        if (lane == 0) next = atomicAdd(ctr, 1ull);
+        const int64_t v = ch * 32 + lane;
+        // every rank's values of this vector, loads issued together
+        uint32_t wd[P][4];
+        if (v < nvec_full) {
 #pragma unroll
-                for (int r = 0; r < P; ++r) {
-                    const uint4 x = ld_stream(reinterpret_cast<const uint4 *>(src.g[r]) + v);
-                    wd[r][0] = x.x, wd[r][1] = x.y, wd[r][2] = x.z, wd[r][3] = x.w;
+            for (int r = 0; r < P; ++r) {
+                const uint4 x = ld_stream(reinterpret_cast<const uint4 *>(src.g[r]) + v);
+                wd[r][0] = x.x, wd[r][1] = x.y, wd[r][2] = x.z, wd[r][3] = x.w;
+            }
+        } else {
+#pragma unroll
+            for (int r = 0; r < P; ++r) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) wd[r][q] = 0u;
+                if (v < nvec_all) {
+#pragma unroll
+                    for (int j = 0; j < kQnVec; ++j)
+                        if (v * kQnVec + j < n) wd[r][j >> 1] |= uint32_t(src.g[r][v * kQnVec + j]) << (16 * (j & 1));
+                }
+            }
+        }
+        float2 g2[kQnVec / 2];
+#pragma unroll
+        for (int q = 0; q < kQnVec / 2; ++q) g2[q] = make_float2(0.0f, 0.0f);
+#pragma unroll
+        for (int r = 0; r < P; ++r) {
+            uint32_t pairs[4];
+            const uint32_t sbyte = mx_encode_slice<4>(wd[r], pairs);
+            if (v < nvec_full) {
+                __stcs(reinterpret_cast<uint2 *>(out.c[r]) + v,
+                       make_uint2(pairs[0] | (pairs[1] << 16), pairs[2] | (pairs[3] << 16)));
+            } else if (v < nvec_all) {
+#pragma unroll
+                for (int j = 0; j < kQnVec; ++j)
+                    if (v * kQnVec + j < n) out.c[r][v * kQnVec + j] = uint8_t(pairs[j >> 1] >> (8 * (j & 1)));
+            }
+            if ((lane & 3) == 0 && v < nvec_all) out.s[r][v >> 2] = uint8_t(sbyte);
+            // the decoded payload, summed in rank order
+            const float scale = e8m0_value(sbyte);
+            const float2 s2 = make_float2(scale, scale);
+#pragma unroll
+            for (int q = 0; q < kQnVec / 2; ++q) g2[q] = fma_f32x2(e4m3x2_to_f32x2(uint16_t(pairs[q])), s2, g2[q]);
+        }
+        // unscale, square in fp32, the lane's two-sum pair in element order
+        // (vectors past the end hold zeros: their squares are +0)
+        float g[kQnVec];
+        float hi = 0.0f, lo = 0.0f;
+#pragma unroll
+        for (int q = 0; q < kQnVec / 2; ++q) {
+            g2[q] = mul_f32x2(g2[q], inv2);
+            g[2 * q] = g2[q].x;
+            g[2 * q + 1] = g2[q].y;
+            const float2 sq = mul_f32x2(g2[q], g2[q]);
+            two_sum_acc(hi, lo, sq.x);
+            two_sum_acc(hi, lo, sq.y);
+        }
+        if (kStage && v < nvec_all) {
+            // the reduce-scatter output for the staged step pass
+            if (v < nvec_full) {
+                float4 *o = reinterpret_cast<float4 *>(stage) + 2 * v;
+                const float4 a = make_float4(g[0], g[1], g[2], g[3]);
+                const float4 b = make_float4(g[4], g[5], g[6], g[7]);
+                if (v >= nvec_full - kStageKeepBytes / 32) {
+                    o[0] = a;
+                    o[1] = b;
+                } else {
+                    __stcs(o, a);
+                    __stcs(o + 1, b);
                 }
             } else {
 #pragma unroll
-                for (int r = 0; r < P; ++r) {
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) wd[r][q] = 0u;
-                    if (v < nvec_all) {
-#pragma unroll
-                        for (int j = 0; j < kQnVec; ++j)
-                            if (v * kQnVec + j < n) wd[r][j >> 1] |= uint32_t(src.g[r][v * kQnVec + j]) << (16 * (j & 1));
-                    }
-                }
-            }
-            float2 g2[kQnVec / 2];
-#pragma unroll
-            for (int q = 0; q < kQnVec / 2; ++q) g2[q] = make_float2(0.0f, 0.0f);
-#pragma unroll
-            for (int r = 0; r < P; ++r) {
-                uint32_t pairs[4];
-                const uint32_t sbyte = mx_encode_slice<4>(wd[r], pairs);
-                if (v < nvec_full) {
-                    __stcs(reinterpret_cast<uint2 *>(out.c[r]) + v,
-                           make_uint2(pairs[0] | (pairs[1] << 16), pairs[2] | (pairs[3] << 16)));
-                } else if (v < nvec_all) {
-#pragma unroll
-                    for (int j = 0; j < kQnVec; ++j)
-                        if (v * kQnVec + j < n) out.c[r][v * kQnVec + j] = uint8_t(pairs[j >> 1] >> (8 * (j & 1)));
-                }
-                if ((lane & 3) == 0 && v < nvec_all) out.s[r][v >> 2] = uint8_t(sbyte);
-                // the decoded payload, summed in rank order
-                const float scale = e8m0_value(sbyte);
-                const float2 s2 = make_float2(scale, scale);
-#pragma unroll
-                for (int q = 0; q < kQnVec / 2; ++q) g2[q] = fma_f32x2(e4m3x2_to_f32x2(uint16_t(pairs[q])), s2, g2[q]);
-            }
-            // unscale, square in fp32, add every square with two-sum (vectors
-            // past the end hold zeros: their squares are +0)
-#pragma unroll
-            for (int q = 0; q < kQnVec / 2; ++q) {
-                g2[q] = mul_f32x2(g2[q], inv2);
-                const float2 sq = mul_f32x2(g2[q], g2[q]);
-                two_sum_acc(hi, lo, sq.x);
-                two_sum_acc(hi, lo, sq.y);
-            }
-            if (kStage && v < nvec_all) {
-                // the reduce-scatter output for the staged step pass
-                if (v < nvec_full) {
-                    float4 *o = reinterpret_cast<float4 *>(stage) + 2 * v;
-                    const float4 a = make_float4(g2[0].x, g2[0].y, g2[1].x, g2[1].y);
-                    const float4 b = make_float4(g2[2].x, g2[2].y, g2[3].x, g2[3].y);
-                    if (v >= nvec_full - kStageKeepBytes / 32) {
-                        o[0] = a;
-                        o[1] = b;
-                    } else {
-                        __stcs(o, a);
-                        __stcs(o + 1, b);
-                    }
-                } else {
-#pragma unroll
-                    for (int j = 0; j < kQnVec; ++j)
-                        if (v * kQnVec + j < n) stage[v * kQnVec + j] = (j & 1) ? g2[j >> 1].y : g2[j >> 1].x;
-                }
+                for (int j = 0; j < kQnVec; ++j)
+                    if (v * kQnVec + j < n) stage[v * kQnVec + j] = g[j];
             }
         }
-        // the codes and scale bytes of this run are written; the non-finite
-        // case below reads them back (another lane of the block wrote the
-        // scale byte)
-        __syncwarp();
-        if (isfinite(hi) && isfinite(lo)) {
-            acc += double(hi);
-            acc += double(lo);
-        } else {
-            // a square that is not finite, or a run whose fp32 partial
-            // overflowed: redo the run with every square widened to fp64 on
-            // its own, from the payload
-            MxSrc<P> mx;
-#pragma unroll
-            for (int r = 0; r < P; ++r) {
-                mx.c[r] = out.c[r];
-                mx.s[r] = out.s[r];
-            }
-#pragma unroll 1
-            for (int k = 0; k < kQnRun; ++k) {
-                const int64_t v = row + k * stride + lane;
-                if (v >= nvec_all) break;
-#pragma unroll 1
-                for (int j = 0; j < kQnVec; ++j) {
-                    const int64_t i = v * kQnVec + j;
-                    if (i >= n) break;
-                    const float g = __fmul_rn(mx.sum1(i), inv);
-                    acc += double(__fmul_rn(g, g));
-                }
-            }
-        }
+        chunk_add(hi, lo, g, lane, word, flags);
+        next = __shfl_sync(0xffffffffu, next, 0);
+        ch = wq + int64_t(kWorkLanes) * (int64_t(gridDim.x) + int64_t(next));
     }
-    norm_finish(acc, partials, sc, fk, kNormWhole);
+    norm_exact_finish(word, flags, work, sc, fk, kNormWhole);
 }
 
 cudaError_t launch_quant_norm(int p, const uint16_t *const *g, uint8_t *const *codes, uint8_t *const *scales,
-                              int64_t n, float inv, double *partials, int max_blocks, Scalars *sc, FinalizeK fk,
+                              int64_t n, float inv, unsigned long long *work, Scalars *sc, FinalizeK fk,
                               cudaStream_t st, float *stage)
 {
     return with_ranks(p, [&](auto rk) {
@@ -178,12 +157,13 @@ cudaError_t launch_quant_norm(int p, const uint16_t *const *g, uint8_t *const *c
             out.s[r] = scales[r];
         }
         auto *kernel = stage ? &quant_norm_kernel<P, true> : &quant_norm_kernel<P, false>;
-        const int64_t nvec = (n + kQnVec - 1) / kQnVec;
-        const int64_t want = (nvec + kNormThreads - 1) / kNormThreads;
-        int blocks = int(want < 1 ? 1 : (want < max_blocks ? want : max_blocks));
+        // warp chunks of 32 vectors: no more blocks than give every warp one,
+        // no more than one wave
+        const int64_t chunks = ((n + kQnVec - 1) / kQnVec + 31) / 32;
+        const int64_t want = (chunks + kNormThreads / 32 - 1) / (kNormThreads / 32);
         const int wave = wave_blocks(reinterpret_cast<const void *>(kernel), kNormThreads, 0);
-        if (blocks > wave) blocks = wave;
-        return launch_dependent(kernel, blocks, kNormThreads, 0, st, src, out, n, inv, partials, sc, fk, stage);
+        const int blocks = int(want < 1 ? 1 : (want < wave ? want : wave));
+        return launch_dependent(kernel, blocks, kNormThreads, 0, st, src, out, n, inv, work, sc, fk, stage);
     });
 }
 
