@@ -88,8 +88,8 @@ extern "C" {
                               (one producer warp, consumer warps; tile size chosen by P) */
 #define ZG_VARIANT_STAGED 2 /* the norm pass also stores the reduced fp32 gradient; the step reads it */
 #define ZG_VARIANT_SINGLE 3 /* zg_step runs the norm pass and the fused step in one cooperative launch,
-                              with a grid-wide barrier between them (the norm may differ from the
-                              two-launch norm in its last fp64 bits: its grid is its own) */
+                              with a grid-wide barrier between them (the same norm, decision and
+                              state bits as the two launches) */
 
 typedef struct CUstream_st *zg_stream; /* same type as cudaStream_t */
 typedef struct zg_ctx zg_ctx;          /* opaque; owned by the library */
@@ -112,8 +112,8 @@ typedef struct {
 
 /* Create a context for N parameters over P simulated ranks (1 <= P <= 16,
  * 1 <= N < 2^62) on the current CUDA device. Allocates only a small device
- * workspace (64 KB of fp64 block partials for the MXFP8 and one-launch norm
- * passes, a 4.5 KB work array with the counters the norm and step passes hand
+ * workspace (64 KB of fp64 block partials for the MXFP8 norm pass from
+ * codes, a 4.5 KB work array with the counters the norm and step passes hand
  * out their work with and the norm's exact fixed-point sum, and a 112-byte
  * block of step scalars).
  * Step count starts at 0. Layout: Zero From Scratch, item 17 (one flat
@@ -204,8 +204,9 @@ int zg_shard_step_mxfp8(zg_ctx *ctx, const uint8_t *const *codes, const uint8_t 
  * zg_quant_mxfp8 encodes it, and the global norm, found-inf decision and
  * clip factor are taken from the same codes decoded in registers, exactly as
  * zg_grad_norm_mxfp8 decodes them (its norm agrees with that pass's to
- * rounding: the same per-element values, summed over this kernel's own
- * grid and thread split). Follow it with zg_shard_step_mxfp8 on the same codes
+ * rounding: the same per-element values, summed in another order). It sums
+ * the squares exactly as zg_grad_norm does, so on gradients MXFP8 holds
+ * exactly the two give the same bits. Follow it with zg_shard_step_mxfp8 on the same codes
  * and scales. It reads 2P and writes P(1 + 1/32) bytes per parameter, instead
  * of the P encodes plus a norm pass that reads the P(1 + 1/32) bytes back.
  * With ZG_VARIANT_STAGED it also stores the reduced gradient, as the MX norm

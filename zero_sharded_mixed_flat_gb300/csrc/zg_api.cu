@@ -433,8 +433,7 @@ int zg_step(zg_ctx *ctx, const uint16_t *const *grad_ptrs, float loss_scale, zg_
         if (int rc = check_scale(loss_scale)) return rc;
         if (int rc = check_rank_ptrs(ctx, grad_ptrs, "grad_ptrs", true)) return rc;
         return finish_launch(zg::launch_step_whole(ctx->p, grad_ptrs, ctx->n, inv_scale(ctx, loss_scale), ctx->k,
-                                                   state_of(ctx), ctx->d_sc, ctx->fk, ctx->d_partials,
-                                                   ctx->partials_cap, ctx->wait_limit, stream),
+                                                   state_of(ctx), ctx->d_sc, ctx->fk, ctx->wait_limit, stream),
                              "whole-step launch");
     }
     if (int rc = zg_grad_norm(ctx, grad_ptrs, loss_scale, stream)) return rc;

@@ -305,13 +305,6 @@ struct Bf16Src {
 #endif
     }
 
-    __device__ __forceinline__ void sum8(int64_t vec, float (&out)[kVec]) const
-    {
-        Raw raw;
-        load(vec, raw);
-        reduce(raw, out);
-    }
-
     // Rank-ordered fp32 sums of a loaded vector.
     __device__ __forceinline__ void reduce(const Raw &raw, float (&out)[kVec]) const
     {
@@ -504,10 +497,6 @@ __device__ __forceinline__ void adamw(float g, float c, float bc1, float bc2, co
 // ------------------------------------------------------------------ norm pass
 
 constexpr int kNormThreads = 256;
-#ifndef ZG_NORM_UNROLL
-#define ZG_NORM_UNROLL 1
-#endif
-constexpr int kNormUnroll = ZG_NORM_UNROLL;  // vectors whose loads are in flight together
 
 // Resident blocks per SM the compiler must allow (caps registers per
 // thread): four 256-thread blocks while the P loads of a vector fit in 64
@@ -520,14 +509,12 @@ struct NormMinBlocks {
     static constexpr int value = Src::kRanks <= 8 ? 4 : 2;
 #endif
 };
-constexpr int kNormFlush = 4;  // vectors (32 elements) per two-sum run before widening to fp64
 // The tail of the staged gradient written with the default store policy (see
 // norm_kernel); the rest uses evict-first stores.
 #ifndef ZG_STAGE_KEEP_MB
 #define ZG_STAGE_KEEP_MB 96
 #endif
 constexpr int64_t kStageKeepBytes = int64_t(ZG_STAGE_KEEP_MB) << 20;
-static_assert(kNormFlush % kNormUnroll == 0, "a run holds whole unrolled groups");
 
 // Finalize: runs once, in the last block of the norm pass (thread 0), given
 // the step count and running powers the step passes left in `sc`.
@@ -599,84 +586,6 @@ __device__ __forceinline__ void norm_finish(double acc, double *__restrict__ par
         }
         sc->norm_ticket = 0u;
     }
-}
-
-// One thread's share of the norm pass: grid-stride over 8-element vectors
-// from vector `v` (stride `stride`), g squared in fp32, runs of 32 squares
-// added with two-sum and widened to fp64; block 0's thread 0 also takes the
-// ragged tail. The set of vectors, and so the sum, is a function of N, the
-// thread's index and the grid only.
-template <class Src, bool kStage>
-__device__ __forceinline__ double norm_thread_sum(const Src &src, int64_t n, float inv, float *__restrict__ stage,
-                                                  int64_t v, int64_t stride)
-{
-    const int64_t nvec = n / kVec;
-    double acc = 0.0;
-    while (v < nvec) {
-        const int64_t run_start = v;
-        float hi = 0.0f, lo = 0.0f;
-#pragma unroll 1
-        for (int k = 0; k < kNormFlush && v < nvec; k += kNormUnroll, v += kNormUnroll * stride) {
-            typename Src::Raw raw[kNormUnroll];
-#pragma unroll
-            for (int u = 0; u < kNormUnroll; ++u)
-                if (v + u * stride < nvec) src.load_norm(v + u * stride, raw[u]);
-#pragma unroll
-            for (int u = 0; u < kNormUnroll; ++u) {
-                if (v + u * stride >= nvec) break;
-                float gh[kVec];
-                src.reduce(raw[u], gh);
-#pragma unroll
-                for (int j = 0; j < kVec; ++j) {
-                    gh[j] = __fmul_rn(gh[j], inv);
-                    two_sum_acc(hi, lo, __fmul_rn(gh[j], gh[j]));
-                }
-                if (kStage) {
-                    // keep the reduce-scatter output for the step pass. Its
-                    // last kStageKeepBytes (the part the step pass, walking
-                    // from the end, reads first) get the default store policy
-                    // so they can still be in L2; the rest streams out.
-                    const int64_t vv = v + u * stride;
-                    float4 *o = reinterpret_cast<float4 *>(stage) + 2 * vv;
-                    const float4 a = make_float4(gh[0], gh[1], gh[2], gh[3]);
-                    const float4 b = make_float4(gh[4], gh[5], gh[6], gh[7]);
-                    if (vv >= nvec - kStageKeepBytes / 32) {
-                        o[0] = a;
-                        o[1] = b;
-                    } else {
-                        __stcs(o, a);
-                        __stcs(o + 1, b);
-                    }
-                }
-            }
-        }
-        if (isfinite(hi) && isfinite(lo)) {
-            acc += double(hi);
-            acc += double(lo);
-        } else {
-            // Rare: a run whose fp32 partial overflowed or met inf/NaN. Redo
-            // it with every square widened to fp64 on its own, so the result
-            // is non-finite exactly when some square is.
-#pragma unroll 1
-            for (int64_t u = run_start; u < v && u < nvec; u += stride) {
-                float gh[kVec];
-                src.sum8(u, gh);
-#pragma unroll
-                for (int j = 0; j < kVec; ++j) {
-                    const float g = __fmul_rn(gh[j], inv);
-                    acc += double(__fmul_rn(g, g));
-                }
-            }
-        }
-    }
-    if (blockIdx.x == 0 && threadIdx.x == 0) {
-        for (int64_t i = nvec * kVec; i < n; ++i) {  // ragged tail, fewer than 8 elements
-            const float g = __fmul_rn(src.sum1(i), inv);
-            acc += double(__fmul_rn(g, g));
-            if (kStage) stage[i] = g;
-        }
-    }
-    return acc;
 }
 
 // ------------------------------------------------------------------ exact, order-free norm sum
@@ -868,13 +777,11 @@ __device__ __forceinline__ void norm_chunk_loop(const Src &src, int64_t n, float
     }
 }
 
-// The end of the norm pass: the block's digits and flags go into the work
-// array; the last block to finish (an atomic ticket) takes the words (and
-// clears them, the flags and the norm counters for the next launch), rounds
-// the sum to binary64 and writes the decision (or, for a bucket, adds to the
-// running bucket sum).
-__device__ __forceinline__ void norm_exact_finish(long long word, uint32_t flags, unsigned long long *work,
-                                                  Scalars *sc, const FinalizeK &fk, int mode)
+// The end of a block's share of the norm: its digits and flags go into the
+// work array, then an atomic ticket. True (in every thread) in the last
+// block to finish.
+__device__ __forceinline__ bool norm_block_publish(long long word, uint32_t flags, unsigned long long *work,
+                                                   Scalars *sc)
 {
     __shared__ long long s_acc[kNormThreads / 32][kAccDigits];
     __shared__ uint32_t s_flags;
@@ -900,7 +807,16 @@ __device__ __forceinline__ void norm_exact_finish(long long word, uint32_t flags
         am_last = (ticket == gridDim.x - 1);
     }
     __syncthreads();
-    if (!am_last || threadIdx.x != 0) return;
+    return am_last != 0;
+}
+
+// The last block's thread 0: takes the words (and clears them, the flags and
+// the norm counters for the next launch), rounds the sum to binary64 and
+// writes the decision (or, for a bucket, adds to the running bucket sum).
+// The caller resets the ticket.
+__device__ __forceinline__ void norm_total_decide(unsigned long long *work, Scalars *sc, const FinalizeK &fk,
+                                                  int mode)
+{
     __threadfence();
     // what the decision needs besides the sum, read while the words are fetched
     const int64_t t = sc->t;
@@ -923,6 +839,13 @@ __device__ __forceinline__ void norm_exact_finish(long long word, uint32_t flags
         sc->bucket_acc = run;
         if (mode & kNormLast) finalize_decision(sc, run, fk, t, b1p, b2p);
     }
+}
+
+__device__ __forceinline__ void norm_exact_finish(long long word, uint32_t flags, unsigned long long *work,
+                                                  Scalars *sc, const FinalizeK &fk, int mode)
+{
+    if (!norm_block_publish(word, flags, work, sc) || threadIdx.x != 0) return;
+    norm_total_decide(work, sc, fk, mode);
     sc->norm_ticket = 0u;
 }
 
@@ -1487,6 +1410,7 @@ __global__ void __launch_bounds__(ws_threads(TILE), ZG_TMA_WS_MINB)
     __shared__ int s_timeout;
     __shared__ int s_stored;  // some consumer of this CTA has written results
     __shared__ long long s_issued;
+    __shared__ long long s_tile[8];  // the tile each buffer holds, -1 after the last
 
     pdl_wait();
     pdl_trigger();
@@ -1498,7 +1422,6 @@ __global__ void __launch_bounds__(ws_threads(TILE), ZG_TMA_WS_MINB)
     const int64_t nvec = n / kVec;
     const int64_t covered = nvec * kVec;  // elements the tiles cover; the rest is the scalar tail
     const int64_t ntiles = (covered + kTile - 1) / kTile;
-    const int64_t my_tiles = int64_t(blockIdx.x) < ntiles ? (ntiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
 
     if (threadIdx.x == 0) {
         s_timeout = 0;
@@ -1513,27 +1436,35 @@ __global__ void __launch_bounds__(ws_threads(TILE), ZG_TMA_WS_MINB)
     __syncthreads();
 
     auto stage_ptr = [&](int s) { return smem + size_t(s) * lay.stage_bytes; };
-    // first element of this CTA's j-th tile; the tiles are walked from the
-    // end, like the plain kernel's vectors, where the norm pass finished
-    auto tile_start = [&](int64_t j) {
-        const int64_t t = int64_t(blockIdx.x) + j * gridDim.x;
-        return (ZG_TMA_REVERSE ? ntiles - 1 - t : t) * kTile;
-    };
+    // first element of tile t; the tiles are walked from the end, like the
+    // plain kernel's vectors, where the norm pass finished
+    auto tile_start = [&](int64_t t) { return (ZG_TMA_REVERSE ? ntiles - 1 - t : t) * kTile; };
     const volatile int *abort = &s_timeout;
     const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
 
     if (skip == 0 && warp == kConsumers / 32) {
-        // producer: one lane issues every copy of this CTA's tiles in order
+        // producer: one lane issues every copy of this CTA's tiles in order.
+        // The CTA's first tile is its index; each further one comes from a
+        // counter (grid + its next value), so CTAs whose copies land sooner
+        // take more tiles and the launch ends together. After the last tile
+        // the next buffer gets the index -1 and a plain arrival.
         if (lane == 0) {
             int64_t j = 0;
-            for (; j < my_tiles; ++j) {
+            int64_t t = blockIdx.x;
+            for (;; ++j) {
                 const int s = int(j % stages);
                 if (j >= stages &&
                     !mbar_wait_or_abort(&empty[s], uint32_t(((j / stages) - 1) & 1), wait_limit, abort)) {
                     atomicExch(&s_timeout, 1);
                     break;
                 }
-                const int64_t t0 = tile_start(j);
+                if (t >= ntiles) {
+                    s_tile[s] = -1;
+                    mbar_arrive(&full[s]);
+                    break;
+                }
+                s_tile[s] = t;
+                const int64_t t0 = tile_start(t);
                 const int64_t len = covered - t0 < kTile ? covered - t0 : kTile;
                 unsigned char *buf = stage_ptr(s);
                 const uint32_t gb = uint32_t(len * 2), fb = uint32_t(len * 4);
@@ -1544,11 +1475,12 @@ __global__ void __launch_bounds__(ws_threads(TILE), ZG_TMA_WS_MINB)
                 bulk_g2s(f, st.w + t0, fb, &full[s]);
                 bulk_g2s(f + kTile, st.m + t0, fb, &full[s]);
                 bulk_g2s(f + 2 * kTile, st.v + t0, fb, &full[s]);
+                t = int64_t(gridDim.x) + int64_t(atomicAdd(st.work + kStepCtr, 1ull));
             }
-            s_issued = j;
+            s_issued = j;  // buffers with copies in flight or landed (not the -1 one)
         }
     } else if (skip == 0) {
-        for (int64_t j = 0; j < my_tiles; ++j) {
+        for (int64_t j = 0;; ++j) {
             const int s = int(j % stages);
             // one decision per warp, so no lane leaves while the others sync
             const bool ok = __all_sync(0xffffffffu, mbar_wait_or_abort(&full[s], uint32_t((j / stages) & 1),
@@ -1557,7 +1489,9 @@ __global__ void __launch_bounds__(ws_threads(TILE), ZG_TMA_WS_MINB)
                 if (lane == 0) atomicExch(&s_timeout, 1);
                 break;
             }
-            const int64_t t0 = tile_start(j);
+            const long long tile = *reinterpret_cast<volatile long long *>(&s_tile[s]);
+            if (tile < 0) break;  // the producer has no more tiles
+            const int64_t t0 = tile_start(tile);
             const int64_t len = covered - t0 < kTile ? covered - t0 : kTile;
             const int e = threadIdx.x * kVec;
             const bool active = e < len;
@@ -1652,6 +1586,7 @@ __global__ void __launch_bounds__(ws_threads(TILE), ZG_TMA_WS_MINB)
                 }
                 sc->step_gen = sc->norm_gen;
             }
+            st.work[kStepCtr] = 0ull;  // every producer has taken its last tile
             sc->step_ticket = 0u;
         }
     }

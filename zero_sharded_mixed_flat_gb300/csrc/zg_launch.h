@@ -33,8 +33,7 @@ cudaError_t launch_step_tma(int p, const uint16_t *const *g, int64_t n, float in
 // The whole bf16 step (norm pass, grid barrier, step pass) in one cooperative
 // launch; partials holds at least max_blocks doubles.
 cudaError_t launch_step_whole(int p, const uint16_t *const *g, int64_t n, float inv, StepK k, State state,
-                              Scalars *sc, FinalizeK fk, double *partials, int max_blocks, long long wait_limit,
-                              cudaStream_t st);
+                              Scalars *sc, FinalizeK fk, long long wait_limit, cudaStream_t st);
 cudaError_t launch_step_mx(int p, const uint8_t *const *c, const uint8_t *const *s, int64_t n, float inv,
                            StepK k, State state, Scalars *sc, cudaStream_t st);
 cudaError_t launch_quant(const uint16_t *in, int64_t n, uint8_t *codes, uint8_t *scales, cudaStream_t st);

@@ -5,9 +5,12 @@
 // arithmetic, the scale decode and the check for scale bytes the encoder never
 // writes are paid once per sixteen elements. Decoding is issue-bound, not
 // bandwidth-bound (8.25 bytes per parameter at P = 8), which is what this
-// layout buys back. The arithmetic per element is the one norm_kernel uses:
-// the rank-ordered fp32 sum of exact decoded products, times the unscale
-// factor, squared in fp32, added in two-sum runs of 32 squares widened to fp64.
+// layout buys back. Per element: the rank-ordered fp32 sum of exact decoded
+// products, times the unscale factor, squared in fp32. The squares are added
+// in two-sum runs of 32 widened to fp64 over a fixed grid-stride split, not
+// by the bf16 norm pass's exact chunk sum (whose butterfly per 32 vectors
+// this 16-element layout would pay for in issue slots), so the two norms can
+// differ in their last bits (within 1e-12).
 #include "zg_launch.h"
 
 namespace zg {

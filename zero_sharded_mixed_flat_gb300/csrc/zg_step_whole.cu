@@ -2,26 +2,23 @@
 //
 // The clip needs the norm of all N before any update, so the step is two
 // passes over the gradients. Here both run in one cooperative launch: each
-// block takes its share of the norm pass (the same per-thread arithmetic as
-// norm_kernel), writes its block partial and arrives at a grid-wide barrier;
-// the last block to arrive sums the partials in index order, writes the
-// decision (norm, found-inf, clip factor, next bias corrections) and releases
-// the barrier; every block then reads the decision and runs its share of the
-// fused step pass (the same per-thread code as step_kernel). This saves the
-// kernel boundary between the passes and the finalize that the next launch
-// would wait for. The norm depends on the grid, which is this kernel's own
-// (three resident blocks per SM, the step pass's occupancy, against the norm
-// kernel's four), so the norm can differ from the two-launch path's in its
-// last fp64 bits; the state is the same bit for bit whenever the clip factor
-// is.
+// block takes warp chunks of the norm pass (the norm kernel's code: chunks
+// from counters, the exact fixed-point sum), adds its digits into the work
+// array and arrives at a grid-wide barrier; the last block to arrive rounds
+// the sum, writes the decision (norm, found-inf, clip factor, next bias
+// corrections) and releases the barrier; every block then reads the decision
+// and takes warp chunks of the fused step pass (the step kernel's code). This
+// saves the kernel boundary between the passes. The norm is the same exact
+// sum the two-launch path takes, so both give the same bits.
 //
 // The launch is cooperative, so every block is resident and the barrier
 // cannot wait on a block that has not started. Its wait is bounded all the
 // same (wait_limit polls): a block whose wait runs out records
-// ZG_ERR_DEVICE_TIMEOUT and skips its share of the step pass; if some other
-// block had already stored results, the step reports ZG_ERR_STATE_PARTIAL.
-// Every block, the last one included, polls the release at least once, so a
-// limit of 0 makes every block give up before storing anything.
+// ZG_ERR_DEVICE_TIMEOUT and takes no step chunks; if some other block had
+// already stored results, the step reports ZG_ERR_STATE_PARTIAL (the chunks
+// no block took keep their old values). Every block, the last one included,
+// polls the release at least once, so a limit of 0 makes every block give up
+// before storing anything.
 #include "zg_launch.h"
 
 namespace zg {
@@ -56,35 +53,21 @@ struct WholeMinBlocks {
 template <int P>
 __global__ void __launch_bounds__(kStepThreads, WholeMinBlocks<P>::value)
     whole_step_kernel(Bf16Src<P> src, int64_t n, float inv, StepK k, State st, Scalars *sc, FinalizeK fk,
-                      double *__restrict__ partials, long long wait_limit)
+                      long long wait_limit)
 {
     static_assert(kStepThreads == kNormThreads, "one block size for both passes");
-    __shared__ double red[kStepThreads / 32];
-    __shared__ int s_last, s_ok, s_skip;
+    __shared__ int s_ok, s_skip;
     __shared__ float s_c, s_bc1, s_bc2;
-    const int64_t v0 = int64_t(blockIdx.x) * kStepThreads + threadIdx.x;
-    const int64_t stride = int64_t(gridDim.x) * kStepThreads;
 
-    // norm pass: this block's partial, then the barrier
-    const double acc = norm_thread_sum<Bf16Src<P>, false>(src, n, inv, nullptr, v0, stride);
-    const double bsum = block_sum<kStepThreads>(acc, red);
-    if (threadIdx.x == 0) {
-        partials[blockIdx.x] = bsum;
+    // norm pass: this block's chunks, then the barrier
+    long long word = 0;
+    uint32_t flags = 0u;
+    norm_chunk_loop<Bf16Src<P>, false>(src, n, inv, nullptr, st.work, word, flags);
+    if (norm_block_publish(word, flags, st.work, sc) && threadIdx.x == 0) {
+        // the last block: every block's digits are in; round, decide, release
+        norm_total_decide(st.work, sc, fk, kNormWhole);
         __threadfence();
-        s_last = atomicAdd(&sc->norm_ticket, 1u) == gridDim.x - 1;
-    }
-    __syncthreads();
-    if (s_last) {
-        // the last block: every partial is written; sum them in index order
-        __threadfence();
-        double s = 0.0;
-        for (int i = threadIdx.x; i < int(gridDim.x); i += kStepThreads) s += __ldcg(partials + i);
-        const double total = block_sum<kStepThreads>(s, red);
-        if (threadIdx.x == 0) {
-            finalize_decision(sc, total, fk);
-            __threadfence();
-            atomicExch(&sc->norm_ticket, 0u);  // release
-        }
+        atomicExch(&sc->norm_ticket, 0u);  // release
     }
     if (threadIdx.x == 0) {
         s_ok = wait_release(&sc->norm_ticket, wait_limit);
@@ -101,7 +84,7 @@ __global__ void __launch_bounds__(kStepThreads, WholeMinBlocks<P>::value)
     // fused step pass
     bool stored = false;
     if (s_ok && !s_skip) {
-        stored = step_thread_loop(src, n, inv, s_c, s_bc1, s_bc2, k, st, v0, stride);
+        stored = step_chunk_loop(src, n, inv, s_c, s_bc1, s_bc2, k, st);
         if (blockIdx.x == 0 && threadIdx.x == 0 && n % kVec) {
             step_tail(src, n, inv, s_c, s_bc1, s_bc2, k, st);
             stored = true;
@@ -110,7 +93,8 @@ __global__ void __launch_bounds__(kStepThreads, WholeMinBlocks<P>::value)
     const int any_stored = __syncthreads_or(stored);
 
     // commit: the last block of the step counts the step unless it was
-    // skipped or some block's wait ran out, and marks the norm consumed
+    // skipped or some block's wait ran out, marks the norm consumed and
+    // clears the step counters
     if (threadIdx.x == 0) {
         if (!s_ok) {
             sc->status = kStatusTimeout;
@@ -129,24 +113,27 @@ __global__ void __launch_bounds__(kStepThreads, WholeMinBlocks<P>::value)
                 sc->b2p = sc->b2p_next;
             }
             sc->step_gen = sc->norm_gen;
+#pragma unroll
+            for (int q = 0; q < kWorkLanes; ++q) st.work[kStepCtr + q * kWorkStride] = 0ull;
             sc->step_ticket = 0u;
         }
     }
 }
 
 cudaError_t launch_step_whole(int p, const uint16_t *const *g, int64_t n, float inv, StepK k, State state,
-                              Scalars *sc, FinalizeK fk, double *partials, int max_blocks, long long wait_limit,
-                              cudaStream_t st)
+                              Scalars *sc, FinalizeK fk, long long wait_limit, cudaStream_t st)
 {
     return with_ranks(p, [&](auto rk) {
         constexpr int P = decltype(rk)::value;
         Bf16Src<P> src;
         for (int r = 0; r < P; ++r) src.g[r] = g[r];
         auto *kernel = &whole_step_kernel<P>;
-        const int64_t want = (n / kVec + kStepThreads - 1) / kStepThreads;
-        int blocks = int(want < 1 ? 1 : (want < max_blocks ? want : max_blocks));
+        // warp chunks of 32 vectors: no more blocks than give every warp one,
+        // no more than one wave (cooperative: all resident)
+        const int64_t chunks = ((n + kVec - 1) / kVec + 31) / 32;
+        const int64_t want = (chunks + kStepThreads / 32 - 1) / (kStepThreads / 32);
         const int wave = wave_blocks(reinterpret_cast<const void *>(kernel), kStepThreads, 0);
-        if (blocks > wave) blocks = wave;
+        const int blocks = int(want < 1 ? 1 : (want < wave ? want : wave));
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(blocks);
         cfg.blockDim = dim3(kStepThreads);
@@ -157,7 +144,7 @@ cudaError_t launch_step_whole(int p, const uint16_t *const *g, int64_t n, float 
         attr[0].val.cooperative = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        return cudaLaunchKernelEx(&cfg, kernel, src, n, inv, k, state, sc, fk, partials, wait_limit);
+        return cudaLaunchKernelEx(&cfg, kernel, src, n, inv, k, state, sc, fk, wait_limit);
     });
 }
 
