@@ -1199,15 +1199,22 @@ __global__ void __launch_bounds__(kStepThreads, StepMinBlocks<Src>::value)
     float c, bc1, bc2;
     const int skip = step_prologue(sc, c, bc1, bc2);
     if (skip == 0 && kMxOut) {
-        // whole 32-blocks: a warp-uniform loop so four lanes can share a block.
+        // whole 32-blocks in warp chunks of 32 vectors (one per lane), handed
+        // out as in step_chunk_loop, so four neighbouring lanes share a block.
         // Walked from the end like the plain loop: mirroring the index keeps
-        // each four-lane group on one whole block (nvec and base are
-        // multiples of 4), only in reverse lane order.
+        // each four-lane group on one whole block (nvec and the chunk starts
+        // are multiples of 4), only in reverse lane order.
         const int64_t nvec = (n / 32) * 4;
-        const int64_t stride = int64_t(gridDim.x) * kStepThreads;
+        const int64_t nchunk = (nvec + 31) / 32;
         const int lane = threadIdx.x & 31;
+        const int q = threadIdx.x >> 5;
+        unsigned long long *ctr = st.work + kStepCtr + q * kWorkStride;
+        int64_t ch = q + int64_t(kWorkLanes) * blockIdx.x;
 #pragma unroll 1
-        for (int64_t base = int64_t(blockIdx.x) * kStepThreads + (threadIdx.x & ~31); base < nvec; base += stride) {
+        while (ch < nchunk) {  // warp-uniform
+            unsigned long long next = 0ull;
+            if (lane == 0) next = atomicAdd(ctr, 1ull);
+            const int64_t base = ch * 32;
             const bool active = base + lane < nvec;
             const int64_t v = ZG_STEP_REVERSE ? nvec - 1 - (base + lane) : base + lane;
             float w[kVec] = {}, m[kVec], vv[kVec];
@@ -1218,13 +1225,15 @@ __global__ void __launch_bounds__(kStepThreads, StepMinBlocks<Src>::value)
                 store_state(v, st, w, m, vv);
             }
             mx_store_group(v, active, w, st);
+            next = __shfl_sync(0xffffffffu, next, 0);
+            ch = q + int64_t(kWorkLanes) * (int64_t(gridDim.x) + int64_t(next));
         }
         if (blockIdx.x == 0 && threadIdx.x == 0) step_tail_mx(src, n, inv, c, bc1, bc2, k, st);
     } else if (skip == 0) {
         step_chunk_loop(src, n, inv, c, bc1, bc2, k, st);
         if (blockIdx.x == 0 && threadIdx.x == 0) step_tail(src, n, inv, c, bc1, bc2, k, st);
     }
-    step_epilogue(sc, skip, kMxOut ? nullptr : st.work);
+    step_epilogue(sc, skip, st.work);
 }
 
 // ------------------------------------------------------------------ launch
