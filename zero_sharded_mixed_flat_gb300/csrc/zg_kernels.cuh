@@ -1097,33 +1097,6 @@ __device__ __forceinline__ void step_tail(const Src &src, int64_t n, float inv, 
     }
 }
 
-// One thread's share of the fused step pass over the 8-element vectors:
-// grid-stride from `v` (stride `stride`), each vector's index mirrored when
-// ZG_STEP_REVERSE walks from the end, where the norm pass finished (and its
-// last loads may still sit in L2). True when the thread stored anything.
-template <class Src>
-__device__ __forceinline__ bool step_thread_loop(const Src &src, int64_t n, float inv, float c, float bc1, float bc2,
-                                                 const StepK &k, const State &st, int64_t v, int64_t stride)
-{
-    const int64_t nvec = n / kVec;
-    constexpr int U = StepUnroll<Src>::value;
-    const bool any = v < nvec;
-#pragma unroll 1
-    for (; v < nvec; v += U * stride) {
-        VecData<Src> d[U];
-#pragma unroll
-        for (int u = 0; u < U; ++u)
-            if (v + u * stride < nvec)
-                step_load(src, ZG_STEP_REVERSE ? nvec - 1 - (v + u * stride) : v + u * stride, st, d[u]);
-#pragma unroll
-        for (int u = 0; u < U; ++u)
-            if (v + u * stride < nvec)
-                step_compute_store(src, ZG_STEP_REVERSE ? nvec - 1 - (v + u * stride) : v + u * stride, d[u], inv,
-                                   c, bc1, bc2, k, st);
-    }
-    return any;
-}
-
 // One warp's share of the fused step pass, split dynamically. The vectors
 // form chunks of 32 * U (U per lane, lane-consecutive); chunk q + 8j belongs
 // to counter q (the warp's index in its block). A warp's first chunk is fixed
