@@ -500,13 +500,14 @@ constexpr int kNormThreads = 256;
 
 // Resident blocks per SM the compiler must allow (caps registers per
 // thread): four 256-thread blocks while the P loads of a vector fit in 64
-// registers without spilling (P <= 8), two above that.
+// registers without spilling (P = 5..8), three where a lane loads several
+// chunks' vectors at once (P < 5, see NormChunksPerTake), two above P = 8.
 template <class Src>
 struct NormMinBlocks {
 #ifdef ZG_NORM_MINB
     static constexpr int value = ZG_NORM_MINB;
 #else
-    static constexpr int value = Src::kRanks <= 8 ? 4 : 2;
+    static constexpr int value = Src::kRanks > 8 ? 2 : (Src::kRanks >= 5 ? 4 : 3);
 #endif
 };
 // The tail of the staged gradient written with the default store policy (see
@@ -716,64 +717,158 @@ __device__ __forceinline__ void chunk_add(float hi, float lo, const float (&g)[k
     }
 }
 
+// Chunks a warp takes at a time in the norm pass: with few ranks a vector
+// is few bytes, so a lane loads one vector of each of U consecutive chunks
+// before summing any (U * P * 16 bytes in flight per lane: U = 4 at P = 1
+// and 2, 2 at P = 3 and 4, else 1). The chunks, and so the sum, do not
+// change with U.
+template <class Src>
+struct NormChunksPerTake {
+    static constexpr int value = Src::kRanks >= 5 ? 1 : (Src::kRanks >= 3 ? 2 : 4);
+};
+
+// The staged variant's store of vector v's g (the reduce-scatter output the
+// step pass reads). Its last kStageKeepBytes (the part the step pass,
+// walking from the end, reads first) get the default store policy so they
+// can still be in L2; the rest streams out. The partial last vector is
+// stored element by element; vectors past it store nothing.
+__device__ __forceinline__ void norm_stage_store(float *__restrict__ stage, int64_t n, int64_t nfull, int64_t v,
+                                                 const float (&gh)[kVec])
+{
+    if (v < nfull) {
+        float4 *o = reinterpret_cast<float4 *>(stage) + 2 * v;
+        const float4 a = make_float4(gh[0], gh[1], gh[2], gh[3]);
+        const float4 b = make_float4(gh[4], gh[5], gh[6], gh[7]);
+        if (v >= nfull - kStageKeepBytes / 32) {
+            o[0] = a;
+            o[1] = b;
+        } else {
+            __stcs(o, a);
+            __stcs(o + 1, b);
+        }
+    } else if (v * kVec < n) {
+#pragma unroll
+        for (int j = 0; j < kVec; ++j)
+            if (v * kVec + j < n) stage[v * kVec + j] = gh[j];
+    }
+}
+
+// g of chunk `ch` at this lane (its vector, zeros past N), from the loaded
+// raw vector when the vector is whole.
+template <class Src>
+__device__ __forceinline__ void chunk_g(const Src &src, int64_t n, float inv, int64_t ch, int lane,
+                                        const typename Src::Raw &raw, float (&gh)[kVec])
+{
+    const int64_t v = ch * 32 + lane;
+    if (v < n / kVec) {
+        src.reduce(raw, gh);
+    } else {
+#pragma unroll
+        for (int j = 0; j < kVec; ++j) gh[j] = v * kVec + j < n ? src.sum1(v * kVec + j) : 0.0f;
+    }
+#pragma unroll
+    for (int j = 0; j < kVec; ++j) gh[j] = __fmul_rn(gh[j], inv);
+}
+
 // One warp's share of the norm pass over warp chunks (see above), adding
 // into this lane's digit `word` and non-finite flags. The vectors are those
 // of g padded with zeros to a multiple of 8 elements: the last, partial one
-// is read element by element.
+// is read element by element. Work is handed out in takes of U chunks, whose
+// butterflies run side by side; each chunk is added exactly as chunk_add
+// adds it (the same decision between its pair and its squares one by one).
 template <class Src, bool kStage>
 __device__ __forceinline__ void norm_chunk_loop(const Src &src, int64_t n, float inv, float *__restrict__ stage,
                                                 unsigned long long *work, long long &word, uint32_t &flags)
 {
+    constexpr int U = NormChunksPerTake<Src>::value;
     const int64_t nfull = n / kVec;
     const int64_t nvec = (n + kVec - 1) / kVec;
     const int64_t nchunk = (nvec + 31) / 32;
+    const int64_t ntake = (nchunk + U - 1) / U;
     const int lane = threadIdx.x & 31;
     const int q = threadIdx.x >> 5;
     unsigned long long *ctr = work + kNormCtr + q * kWorkStride;
-    int64_t ch = q + int64_t(kWorkLanes) * blockIdx.x;
+    int64_t tk = q + int64_t(kWorkLanes) * blockIdx.x;
+    if constexpr (U == 1) {
 #pragma unroll 1
-    while (ch < nchunk) {  // warp-uniform
-        unsigned long long next = 0ull;
-        if (lane == 0) next = atomicAdd(ctr, 1ull);
-        const int64_t v = ch * 32 + lane;
-        float gh[kVec];
-        float hi = 0.0f, lo = 0.0f;
-        if (v < nfull) {
+        while (tk < ntake) {  // warp-uniform
+            unsigned long long next = 0ull;
+            if (lane == 0) next = atomicAdd(ctr, 1ull);
+            const int64_t v = tk * 32 + lane;
             typename Src::Raw raw;
-            src.load_norm(v, raw);
-            src.reduce(raw, gh);
-        } else {
+            if (v < nfull) src.load_norm(v, raw);
+            float gh[kVec];
+            chunk_g(src, n, inv, tk, lane, raw, gh);
+            float hi = 0.0f, lo = 0.0f;
 #pragma unroll
-            for (int j = 0; j < kVec; ++j) gh[j] = v * kVec + j < n ? src.sum1(v * kVec + j) : 0.0f;
+            for (int j = 0; j < kVec; ++j) two_sum_acc(hi, lo, __fmul_rn(gh[j], gh[j]));
+            if (kStage) norm_stage_store(stage, n, nfull, v, gh);
+            chunk_add(hi, lo, gh, lane, word, flags);
+            next = __shfl_sync(0xffffffffu, next, 0);
+            tk = q + int64_t(kWorkLanes) * (int64_t(gridDim.x) + int64_t(next));
         }
+    } else {
+#pragma unroll 1
+        while (tk < ntake) {  // warp-uniform
+            unsigned long long next = 0ull;
+            if (lane == 0) next = atomicAdd(ctr, 1ull);
+            typename Src::Raw raw[U];
 #pragma unroll
-        for (int j = 0; j < kVec; ++j) {
-            gh[j] = __fmul_rn(gh[j], inv);
-            two_sum_acc(hi, lo, __fmul_rn(gh[j], gh[j]));
-        }
-        if (kStage && v < nfull) {
-            // keep the reduce-scatter output for the step pass. Its last
-            // kStageKeepBytes (the part the step pass, walking from the end,
-            // reads first) get the default store policy so they can still be
-            // in L2; the rest streams out.
-            float4 *o = reinterpret_cast<float4 *>(stage) + 2 * v;
-            const float4 a = make_float4(gh[0], gh[1], gh[2], gh[3]);
-            const float4 b = make_float4(gh[4], gh[5], gh[6], gh[7]);
-            if (v >= nfull - kStageKeepBytes / 32) {
-                o[0] = a;
-                o[1] = b;
-            } else {
-                __stcs(o, a);
-                __stcs(o + 1, b);
+            for (int u = 0; u < U; ++u) {
+                const int64_t v = (tk * U + u) * 32 + lane;
+                if (v < nfull) src.load_norm(v, raw[u]);
             }
-        } else if (kStage && v < nvec) {
+            float hi[U], lo[U];
+            uint32_t fast = 0u;  // chunks whose lanes' pairs are all finite
 #pragma unroll
-            for (int j = 0; j < kVec; ++j)
-                if (v * kVec + j < n) stage[v * kVec + j] = gh[j];
+            for (int u = 0; u < U; ++u) {
+                const int64_t ch = tk * U + u;  // chunks past the end are all zeros
+                const int64_t v = ch * 32 + lane;
+                float gh[kVec];
+                chunk_g(src, n, inv, ch, lane, raw[u], gh);
+                hi[u] = 0.0f;
+                lo[u] = 0.0f;
+#pragma unroll
+                for (int j = 0; j < kVec; ++j) two_sum_acc(hi[u], lo[u], __fmul_rn(gh[j], gh[j]));
+                if (kStage) norm_stage_store(stage, n, nfull, v, gh);
+                fast |= uint32_t(__all_sync(0xffffffffu, isfinite(hi[u]) && isfinite(lo[u]))) << u;
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) {
+#pragma unroll
+                for (int u = 0; u < U; ++u)
+                    pair_add(hi[u], lo[u], __shfl_xor_sync(0xffffffffu, hi[u], off),
+                             __shfl_xor_sync(0xffffffffu, lo[u], off));
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                if (((fast >> u) & 1u) && isfinite(hi[u]) && isfinite(lo[u])) {  // the same in every lane
+                    acc_add(word, hi[u], lane);
+                    acc_add(word, lo[u], lane);
+                } else {
+                    // rare: every square on its own, broadcast from its lane (g
+                    // loaded again, so the raw vectors need not stay in registers)
+                    float gh[kVec];
+                    typename Src::Raw again;
+                    const int64_t v = (tk * U + u) * 32 + lane;
+                    if (v < nfull) src.load_norm(v, again);
+                    chunk_g(src, n, inv, tk * U + u, lane, again, gh);
+#pragma unroll 1
+                    for (int from = 0; from < 32; ++from) {
+#pragma unroll
+                        for (int j = 0; j < kVec; ++j) {
+                            const float x = __shfl_sync(0xffffffffu, __fmul_rn(gh[j], gh[j]), from);
+                            if (isfinite(x))
+                                acc_add(word, x, lane);
+                            else
+                                flags |= isnan(x) ? 2u : 1u;
+                        }
+                    }
+                }
+            }
+            next = __shfl_sync(0xffffffffu, next, 0);
+            tk = q + int64_t(kWorkLanes) * (int64_t(gridDim.x) + int64_t(next));
         }
-        chunk_add(hi, lo, gh, lane, word, flags);
-        next = __shfl_sync(0xffffffffu, next, 0);
-        ch = q + int64_t(kWorkLanes) * (int64_t(gridDim.x) + int64_t(next));
     }
 }
 

@@ -183,10 +183,13 @@ extern "C" int zg_grad_norm_noalloc(const uint16_t *const *grad_ptrs, int p, int
         int wave = 0;
         cudaError_t err = wave_of<P>(dev, &wave);
         if (err != cudaSuccess) return err;
-        // warp chunks of 32 vectors: no more blocks than give every warp one,
-        // no more than one wave (the sum does not depend on the grid)
-        const int64_t chunks = (n / zg::kVec + 31) / 32;
-        const int64_t want = (chunks + zg::kNormThreads / 32 - 1) / (zg::kNormThreads / 32);
+        // warp chunks of 32 vectors taken a few at a time: no more blocks than
+        // give every warp a take, no more than one wave (the sum does not
+        // depend on the grid)
+        constexpr int kPerTake = zg::NormChunksPerTake<zg::Bf16Src<P>>::value;
+        const int64_t chunks = ((n + zg::kVec - 1) / zg::kVec + 31) / 32;
+        const int64_t takes = (chunks + kPerTake - 1) / kPerTake;
+        const int64_t want = (takes + zg::kNormThreads / 32 - 1) / (zg::kNormThreads / 32);
         int64_t blocks = want < 1 ? 1 : want;
         if (blocks > wave) blocks = wave;
         zg::Bf16Src<P> src;
