@@ -42,6 +42,7 @@ import ctypes
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -168,12 +169,19 @@ def measured_peaks() -> tuple[float, str]:
 
 
 def kernel_source_hash() -> str:
+    """A hash of the CUDA sources with their comments and blank space taken
+    out, so that ncu counters stay attached to the code they were taken on
+    while a comment is corrected."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "zero_sharded_mixed_flat_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
         if f.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, f), "rb") as fh:
-                h.update(fh.read())
+            with open(os.path.join(csrc, f), encoding="utf-8") as fh:
+                text = fh.read()
+            text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)  # block comments
+            text = re.sub(r"//[^\n]*", "", text)                # line comments (no string in these sources holds //)
+            h.update(f.encode())
+            h.update(" ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 

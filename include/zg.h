@@ -339,7 +339,7 @@ int zg_probe_copy(const void *src, void *dst, int64_t bytes, zg_stream stream);
  * grad_average 0 or 1. Other values are rejected with ZG_ERR_INVALID_ARG or
  * ZG_ERR_MISALIGNED and a message in zg_last_error.
  * It allocates nothing: no cudaMalloc, no cudaFree, no allocating library
- * call. Its scratch is a fixed 4,864-byte array inside the library's device
+ * call. Its scratch is a fixed 4,736-byte array inside the library's device
  * image (a result block and the norm pass's work array); every GPU that loads
  * the library holds that array until the process exits. The first call on a device looks up the array's
  * device address (cudaGetSymbolAddress), so make that first call before any

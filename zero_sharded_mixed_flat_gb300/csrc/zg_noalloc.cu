@@ -42,7 +42,7 @@
 namespace {
 
 constexpr size_t kResultBytes = 256;  // the scalar block (result + counter), padded to keep the work array aligned
-constexpr size_t kScratchBytes = kResultBytes + zg::kWorkWords * sizeof(unsigned long long);  // 4,864 bytes
+constexpr size_t kScratchBytes = kResultBytes + zg::kWorkWords * sizeof(unsigned long long);  // 4,736 bytes
 static_assert(sizeof(zg::Scalars) <= kResultBytes, "the scalar block must fit in front of the work array");
 static_assert(offsetof(zg::Scalars, sumsq) == 0 && offsetof(zg::Scalars, norm) == sizeof(double),
               "the result copy takes sumsq and norm as the first 16 bytes");
