@@ -79,6 +79,27 @@ def test_roofline_bookkeeping(monkeypatch, tmp_path):
     assert bench.recorded_traffic("zg_shard_step", "missing") is None
 
 
+def test_source_hash_ignores_comments_only(monkeypatch, tmp_path):
+    """The hash that ties ncu counters to the kernel sources changes with the
+    code, not with a corrected comment or re-wrapped blank space."""
+    real = os.path.join(bench.ROOT, "zero_sharded_mixed_flat_gb300", "csrc")
+    csrc = tmp_path / "zero_sharded_mixed_flat_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    for f in os.listdir(real):
+        if f.endswith((".cu", ".cuh", ".h")):
+            (csrc / f).write_text(open(os.path.join(real, f), encoding="utf-8").read(), encoding="utf-8")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    base = bench.kernel_source_hash()
+    target = csrc / "zg_gather.cu"
+    text = target.read_text(encoding="utf-8")
+    target.write_text(text.replace("// ", "//  a reworded note: ", 3) + "\n/* a closing remark */\n\n",
+                      encoding="utf-8")
+    assert bench.kernel_source_hash() == base
+    target.write_text(text.replace("constexpr int kGatherUnroll = 4;", "constexpr int kGatherUnroll = 2;"),
+                      encoding="utf-8")
+    assert bench.kernel_source_hash() != base
+
+
 def test_threaded_oracle_matches_the_oracle():
     """The bench's many-thread oracle timing runs the oracle's own range
     functions; its state after a few steps equals the one-thread oracle's
