@@ -143,7 +143,9 @@ int zg_step(zg_ctx *ctx, const uint16_t *const *grad_ptrs, float loss_scale, zg_
  * partial sums rounded once to binary64, so the result does not depend on
  * how the work was spread over the GPU), the found-inf decision, the clip
  * factor and the next bias corrections, all left in device memory. Reads 2P
- * bytes per parameter. */
+ * bytes per parameter. The exact sum's 64-bit digit words hold any N below
+ * 2^38 (2.7e11 elements; a rank's bf16 gradient of that length would need
+ * 550 GB of device memory). */
 int zg_grad_norm(zg_ctx *ctx, const uint16_t *const *grad_ptrs, float loss_scale, zg_stream stream);
 
 /* The first half of a step taken bucket by bucket, so each bucket's share of
